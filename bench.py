@@ -1,0 +1,443 @@
+"""Benchmark: one step = route preprocessing + forward + backward of exact
+route-set sparse GQA attention on the right-padded block-route workload
+(B=2, S_q=S_kv=4096, Hq=16, Hkv=2, D=256, K=2048 int32 routes), BF16.
+
+Prints ONE JSON line (rank 0).  ``value`` is useful TFLOP/s over deduplicated
+valid routes: forward 4*Hq*D*K_eff and backward 10*Hq*D*K_eff FLOP per query
+row, divided by the device time of the step with inputs already in HBM.  The
+L2 cache is flushed (a 256 MiB write) before every timed step, outside the
+timed events.  ``e2e`` is the same metric through the public API with pinned
+host buffers: host->device copies of Q, K, V, dO and the routes and
+device->host copies of O, LSE, dQ, dK, dV are inside its timed region.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload, on the host cores.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path needs no exchange); the barrier and the max-over-ranks timing use
+torch.distributed, nothing on the data path does.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from route_sparse_gqa_gb300 import workloads as W  # noqa: E402
+
+METRIC = "route-sparse GQA fwd+bwd useful TFLOP/s on 1 GB300; % of roofline"
+UNIT = "TFLOP/s"
+FLOP_FWD_PER_KEY = 4   # x Hq x D per valid (row, key)
+FLOP_BWD_PER_KEY = 10  # x Hq x D: S recompute, dP, dV, dQ, dK matmuls
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def work_counts(w, counts: np.ndarray):
+    keff = int(counts.astype(np.int64).sum())
+    rows = int((counts > 0).sum())
+    D = w.D
+    return {
+        "keff_total": keff,
+        "rows_nonempty": rows,
+        "fwd_flop": FLOP_FWD_PER_KEY * w.Hq * D * keff,
+        "bwd_flop": FLOP_BWD_PER_KEY * w.Hq * D * keff,
+        # Algorithmic bytes (per query row): gathered bf16 K and V rows of every routed key for each KV head,
+        # plus the row's own Q read / O write / LSE write (forward) or Q, dO read and dQ write plus LSE and
+        # Delta reads (backward); backward also scatter-adds fp32 dK and dV (8 bytes per routed element).
+        "fwd_bytes": 4 * w.Hkv * D * keff + rows * (w.Hq * D * 4 + 4 * w.Hq),
+        "bwd_bytes": 12 * w.Hkv * D * keff + rows * (w.Hq * D * 6 + 8 * w.Hq),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qsa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "route_sparse_gqa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(kernel)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+def make_device_inputs(case, device):
+    import torch
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    return bf(case.q), bf(case.k), bf(case.v), bf(case.do), torch.from_numpy(case.routes).to(device)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import route_sparse_gqa_gb300 as qsa
+    from route_sparse_gqa_gb300 import build as qbuild
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qbuild.build()
+    w = W.WORKLOADS[args.workload]
+    case = W.make_case(args.workload)
+    q, k, v, do, routes = make_device_inputs(case, dev)
+    scale = w.softmax_scale
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+
+    def step(timers=None):
+        if timers:
+            timers[0].record()
+        plan = qsa.preprocess(q, k, v, routes, scale)
+        if timers:
+            timers[1].record()
+        o, lse = qsa.forward(plan, q, k, v)
+        if timers:
+            timers[2].record()
+        dq, dk, dv = qsa.backward(plan, q, k, v, o, lse, do)
+        if timers:
+            timers[3].record()
+        return plan, o, lse, dq, dk, dv
+
+    plan, *_ = step()
+    _, counts = plan.route_sets()
+    plan.device_status()
+    wc = work_counts(w, counts.cpu().numpy())
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # L2 flush between timed steps, outside the events
+            step(events[i])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(3)] for i in range(args.steps)])
+    step_ms = float(per.sum(1).sum() / args.steps)
+    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms_max = float(t.item())
+    pre_ms, fwd_ms, bwd_ms = (float(x) for x in per.mean(0))
+    plan.device_status()
+
+    flop_step = wc["fwd_flop"] + wc["bwd_flop"]
+    value = flop_step * world / (step_ms_max * 1e-3) / 1e12
+
+    # End to end through the public API with pinned host buffers.
+    e2e = run_e2e(case, w, dev, args, qsa, flop_step, world)
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    fwd_gbs = wc["fwd_bytes"] / (fwd_ms * 1e-3) / 1e9
+    bwd_gbs = wc["bwd_bytes"] / (bwd_ms * 1e-3) / 1e9
+    dominant = "backward" if bwd_ms >= fwd_ms else "forward"
+    kern = {"forward": ("qsa_forward", fwd_gbs, wc["fwd_bytes"], fwd_ms),
+            "backward": ("qsa_backward", bwd_gbs, wc["bwd_bytes"], bwd_ms)}[dominant]
+    roofline = {
+        "bound": "hbm",
+        "achieved": round(kern[1], 1),
+        "peak": hbm,
+        "unit": "GB/s",
+        "frac": round(kern[1] / hbm, 4),
+        "traffic": recorded_traffic(kern[0]),
+        "kernel": kern[0],
+        "algorithmic_bytes_per_launch": kern[2],
+        "launch_ms": round(kern[3], 4),
+        "peak_source": f"{peak_src} MEASURED_PEAKS.json hbm_gbs" if peak_src == "measured" else "fallback",
+        "fwd_frac": round(fwd_gbs / hbm, 4),
+        "bwd_frac": round(bwd_gbs / hbm, 4),
+        "fwd_tflops": round(wc["fwd_flop"] / (fwd_ms * 1e-3) / 1e12, 2),
+        "bwd_tflops": round(wc["bwd_flop"] / (bwd_ms * 1e-3) / 1e12, 2),
+        "fwd_tensor_frac": round(wc["fwd_flop"] / (fwd_ms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4),
+        "bwd_tensor_frac": round(wc["bwd_flop"] / (bwd_ms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4),
+    }
+    cpu = run_cpu_baseline(case, w, args) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{w.name}: {w.summary}",
+            "step": "preprocess + forward + backward (fp32 dK/dV accumulation)",
+            "parallelism": f"replicas x{world}",
+            "l2": "flushed before every timed step (256 MiB write outside the events)",
+            "keff_total": wc["keff_total"],
+            "rows_nonempty": wc["rows_nonempty"],
+            "useful_flop_per_step": flop_step,
+        },
+        "breakdown_ms": {"preprocess": round(pre_ms, 4), "forward": round(fwd_ms, 4), "backward": round(bwd_ms, 4)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * LAUNCHES_PER_STEP,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# libqsa kernels per step: preprocess = route rows + route tiles + tile order,
+# forward = 1, backward = delta + main + dK/dV conversion.
+LAUNCHES_PER_STEP = 7
+
+
+def run_e2e(case, w, dev, args, qsa, flop_step, world):
+    import torch
+
+    host = {}
+    for name in ("q", "k", "v", "do"):
+        bits = np.ascontiguousarray(getattr(case, name)).view(np.int16)
+        host[name] = torch.from_numpy(bits).view(torch.bfloat16).pin_memory()
+    host["routes"] = torch.from_numpy(case.routes).pin_memory()
+    outs = {
+        "o": torch.empty((w.B, w.S_q, w.Hq, w.D), dtype=torch.bfloat16).pin_memory(),
+        "lse": torch.empty((w.B, w.Hq, w.S_q), dtype=torch.float32).pin_memory(),
+        "dq": torch.empty((w.B, w.S_q, w.Hq, w.D), dtype=torch.bfloat16).pin_memory(),
+        "dk": torch.empty((w.B, w.S_kv, w.Hkv, w.D), dtype=torch.bfloat16).pin_memory(),
+        "dv": torch.empty((w.B, w.S_kv, w.Hkv, w.D), dtype=torch.bfloat16).pin_memory(),
+    }
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def step():
+        q = host["q"].to(dev, non_blocking=True)
+        k = host["k"].to(dev, non_blocking=True)
+        v = host["v"].to(dev, non_blocking=True)
+        do = host["do"].to(dev, non_blocking=True)
+        r = host["routes"].to(dev, non_blocking=True)
+        plan = qsa.preprocess(q, k, v, r, w.softmax_scale)
+        o, lse = qsa.forward(plan, q, k, v)
+        dq, dk, dv = qsa.backward(plan, q, k, v, o, lse, do)
+        for name, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            outs[name].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    return {"value": round(flop_step / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def oracle_sample(case, w, rows_per_sample: int, seed: int = 0):
+    """A bounded sample of the workload for the CPU oracle: `rows_per_sample`
+    evenly spaced non-empty query rows of batch row 0, with all their keys."""
+    import oracle
+
+    _, counts = oracle.route_sets(case.routes[:1], w.S_kv)
+    live = np.nonzero(counts[0] > 0)[0]
+    rows = live[np.linspace(0, live.size - 1, min(rows_per_sample, live.size)).astype(np.int64)]
+    f64 = lambda bits: W.bf16_bits_to_f32(bits).astype(np.float64)  # noqa: E731
+    sub = {
+        "q": f64(case.q[:1, rows]), "do": f64(case.do[:1, rows]), "routes": case.routes[:1, rows],
+        "k": f64(case.k[:1]), "v": f64(case.v[:1]),
+    }
+    keff = int(counts[0, rows].astype(np.int64).sum())
+    return sub, rows.size, keff
+
+
+def time_oracle_step(sub, w):
+    import oracle
+
+    t0 = time.perf_counter()
+    o, lse = oracle.forward(sub["q"], sub["k"], sub["v"], sub["routes"], w.softmax_scale)
+    oracle.backward(sub["q"], sub["k"], sub["v"], sub["routes"], sub["do"], w.softmax_scale)
+    return time.perf_counter() - t0
+
+
+def run_cpu_baseline(case, w, args):
+    import oracle
+
+    oracle.build()
+    sub, n_rows, keff = oracle_sample(case, w, args.cpu_rows)
+    secs = time_oracle_step(sub, w)
+    flop = (FLOP_FWD_PER_KEY + FLOP_BWD_PER_KEY) * w.Hq * w.D * keff
+    return {"value": round(flop / secs / 1e12, 6), "unit": UNIT, "cores": oracle.omp_threads(), "kind": "oracle",
+            "seconds": round(secs, 2),
+            "sample": f"{n_rows} evenly spaced non-empty query rows of batch row 0 ({keff} routed keys), "
+                      f"forward + backward with dK/dV over all {w.S_kv} keys, fp64"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    w = W.WORKLOADS[args.workload]
+    case = W.make_case(args.workload)
+    sub, n_rows, keff = oracle_sample(case, w, args.ref_rows)
+    flop = (FLOP_FWD_PER_KEY + FLOP_BWD_PER_KEY) * w.Hq * w.D * keff
+    for _ in range(args.warmup):
+        time_oracle_step(sub, w)
+    secs = [time_oracle_step(sub, w) for _ in range(args.steps)]
+    total = sum(secs)
+    value = flop * args.steps / total / 1e12
+    sample = (f"{n_rows} evenly spaced non-empty query rows of batch row 0 ({keff} routed keys) per step, "
+              f"forward + backward with dK/dV over all {w.S_kv} keys, fp64")
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.summary}", "step": "oracle forward + backward on a bounded sample",
+                   "parallelism": "CPU threads (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": oracle.omp_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, help="workload index (1 = the headline configuration)")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="query rows in the CPU-baseline oracle sample")
+    ap.add_argument("--ref-rows", type=int, default=160, help="query rows per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

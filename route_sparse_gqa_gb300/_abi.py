@@ -1,0 +1,92 @@
+"""ctypes view of libqsa's C ABI (include/qsa.h).  Marshalling only: every step
+of the attention runs in the library's CUDA kernels; nothing here computes."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libqsa.so")
+
+QSA_OK = 0
+STATUS_NAMES = {
+    0: "QSA_OK",
+    1: "QSA_ERR_INVALID_ARGUMENT",
+    2: "QSA_ERR_UNSUPPORTED",
+    3: "QSA_ERR_WORKSPACE_TOO_SMALL",
+    4: "QSA_ERR_CUDA",
+    5: "QSA_ERR_TIMEOUT",
+    6: "QSA_ERR_DEVICE_CHECK",
+}
+
+# Every symbol include/qsa.h declares (checked by the tests against the built library).
+EXPORTS = (
+    "qsa_check_problem",
+    "qsa_workspace_bytes",
+    "qsa_preprocess",
+    "qsa_forward",
+    "qsa_backward",
+    "qsa_copy_route_sets",
+    "qsa_read_device_status",
+    "qsa_status_string",
+    "qsa_last_error",
+)
+
+
+class QSAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = STATUS_NAMES.get(status, f"status {status}")
+        super().__init__(f"{self.status_name}: {message}")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("S_q", ctypes.c_int64), ("S_kv", ctypes.c_int64), ("Hq", ctypes.c_int64),
+        ("Hkv", ctypes.c_int64), ("D", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("route_bits", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+        ("q_stride", ctypes.c_int64 * 4), ("k_stride", ctypes.c_int64 * 4), ("v_stride", ctypes.c_int64 * 4),
+        ("r_stride", ctypes.c_int64 * 3),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Loads the in-tree libqsa.so.  Raises if it has not been built: there is no
+    fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libqsa.so is not built ({LIB_PATH}); run route_sparse_gqa_gb300.build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(Problem)
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        lib.qsa_check_problem.argtypes = [P]
+        lib.qsa_workspace_bytes.argtypes = [P]
+        lib.qsa_workspace_bytes.restype = sz
+        lib.qsa_preprocess.argtypes = [P, vp, vp, sz, vp]
+        lib.qsa_forward.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp]
+        lib.qsa_backward.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.qsa_copy_route_sets.argtypes = [P, vp, sz, vp, vp, vp]
+        lib.qsa_read_device_status.argtypes = [vp, vp]
+        lib.qsa_status_string.argtypes = [ctypes.c_int]
+        lib.qsa_status_string.restype = ctypes.c_char_p
+        lib.qsa_last_error.argtypes = []
+        lib.qsa_last_error.restype = ctypes.c_char_p
+        for name in ("qsa_check_problem", "qsa_preprocess", "qsa_forward", "qsa_backward", "qsa_copy_route_sets",
+                     "qsa_read_device_status"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def check(status: int) -> None:
+    if status != QSA_OK:
+        msg = load().qsa_last_error().decode(errors="replace")
+        raise QSAError(status, msg)

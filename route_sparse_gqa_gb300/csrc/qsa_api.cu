@@ -1,0 +1,379 @@
+// qsa_api.cu -- host side of the libqsa C ABI (include/qsa.h): validation,
+// workspace layout, kernel launches and status reporting.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "qsa_internal.cuh"
+#include "qsa_tc.cuh"
+
+namespace qsa {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+qsa_status fail(qsa_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+qsa_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(QSA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+qsa_status validate(const qsa_problem *p) {
+    if (!p) return fail(QSA_ERR_INVALID_ARGUMENT, "problem is null");
+    if (p->B <= 0 || p->S_q <= 0 || p->S_kv <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->K <= 0)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "every dimension must be positive (B=%lld S_q=%lld S_kv=%lld Hq=%lld "
+                    "Hkv=%lld D=%lld K=%lld)", (long long)p->B, (long long)p->S_q, (long long)p->S_kv,
+                    (long long)p->Hq, (long long)p->Hkv, (long long)p->D, (long long)p->K);
+    if (p->Hq % p->Hkv != 0)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "Hq=%lld is not a multiple of Hkv=%lld", (long long)p->Hq,
+                    (long long)p->Hkv);
+    if (!std::isfinite(p->softmax_scale) || !(p->softmax_scale > 0.f))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "softmax_scale must be finite and positive (got %g)",
+                    (double)p->softmax_scale);
+    if (p->route_bits != 32 && p->route_bits != 64)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "route_bits must be 32 or 64 (got %d)", p->route_bits);
+    if (p->D != kHeadDim) return fail(QSA_ERR_UNSUPPORTED, "head dim D=%lld: only D=256 is supported", (long long)p->D);
+    if (p->S_kv > 2147483647LL) return fail(QSA_ERR_UNSUPPORTED, "S_kv=%lld exceeds 2^31-1", (long long)p->S_kv);
+    if (p->K > kMaxRouteSlots)
+        return fail(QSA_ERR_UNSUPPORTED, "K=%lld route slots exceeds %d", (long long)p->K, kMaxRouteSlots);
+    const int64_t *st[3] = {p->q_stride, p->k_stride, p->v_stride};
+    const char *nm[3] = {"q", "k", "v"};
+    for (int t = 0; t < 3; ++t) {
+        if (st[t][3] != 1) return fail(QSA_ERR_UNSUPPORTED, "%s needs a unit last stride (got %lld)", nm[t],
+                                       (long long)st[t][3]);
+        for (int i = 0; i < 3; ++i)
+            if (st[t][i] < 0 || st[t][i] % 8 != 0)
+                return fail(QSA_ERR_UNSUPPORTED, "%s stride[%d]=%lld must be a non-negative multiple of 8 elements",
+                            nm[t], i, (long long)st[t][i]);
+    }
+    return QSA_OK;
+}
+
+Layout make_layout(const qsa_problem *p) {
+    Layout L{};
+    L.G = p->Hq / p->Hkv;
+    L.T = (is_pow2(L.G) && L.G >= 4 && L.G <= kTileRows) ? kTileRows / L.G : 0;
+    L.n_tiles = L.T ? (p->S_q + L.T - 1) / L.T : 0;
+    const int64_t union_cap = L.T ? std::min<int64_t>(L.T * p->K, p->S_kv) : 0;
+    L.max_chunks = (union_cap + kChunkKeys - 1) / kChunkKeys;
+    const int64_t rows = p->B * p->S_q;
+    const int64_t tiles = p->B * L.n_tiles;
+    size_t off = 0;
+    L.off_status = off;
+    off = align256(off + sizeof(DeviceStatus));
+    L.off_counts = off;
+    off = align256(off + rows * sizeof(int32_t));
+    L.off_ids = off;
+    off = align256(off + rows * p->K * sizeof(int32_t));
+    L.off_tile_nchunks = off;
+    off = align256(off + tiles * sizeof(int32_t));
+    L.off_tile_keys = off;
+    off = align256(off + tiles * L.max_chunks * kChunkKeys * sizeof(int32_t));
+    L.off_tile_masks = off;
+    off = align256(off + tiles * L.max_chunks * L.T * sizeof(uint64_t));
+    L.off_order = off;
+    off = align256(off + tiles * sizeof(int32_t));
+    L.off_delta = off;
+    off = align256(off + p->B * p->Hq * p->S_q * sizeof(float));
+    const size_t kv_f32 = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * sizeof(float);
+    L.off_dk = off;
+    off = align256(off + kv_f32);
+    L.off_dv = off;
+    off = align256(off + kv_f32);
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+template <typename T>
+const T *at(const void *ws, size_t off) {
+    return reinterpret_cast<const T *>(static_cast<const char *>(ws) + off);
+}
+
+qsa_status check_ws(const qsa_problem *p, const void *ws, size_t ws_bytes, Layout &L) {
+    qsa_status st = validate(p);
+    if (st != QSA_OK) return st;
+    if (!ws) return fail(QSA_ERR_INVALID_ARGUMENT, "workspace is null");
+    if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+    L = make_layout(p);
+    if (ws_bytes < L.total)
+        return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, L.total);
+    return QSA_OK;
+}
+
+bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+// [lo, hi) byte range of a strided [B, S, H, D] bf16 tensor.
+void span_of(const void *base, const int64_t *stride, int64_t B, int64_t S, int64_t H, uintptr_t &lo, uintptr_t &hi) {
+    lo = reinterpret_cast<uintptr_t>(base);
+    hi = lo + 2 * (size_t)((B - 1) * stride[0] + (S - 1) * stride[1] + (H - 1) * stride[2] + kHeadDim);
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+AttnArgs attn_args(const qsa_problem *p, const Layout &L, const void *ws, const void *q, const void *k,
+                   const void *v) {
+    AttnArgs a{};
+    a.B = p->B;
+    a.S_q = p->S_q;
+    a.S_kv = p->S_kv;
+    a.Hq = p->Hq;
+    a.Hkv = p->Hkv;
+    a.K = p->K;
+    a.G = L.G;
+    a.scale = p->softmax_scale;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.v = static_cast<const __nv_bfloat16 *>(v);
+    a.qs0 = p->q_stride[0];
+    a.qs1 = p->q_stride[1];
+    a.qs2 = p->q_stride[2];
+    a.ks0 = p->k_stride[0];
+    a.ks1 = p->k_stride[1];
+    a.ks2 = p->k_stride[2];
+    a.vs0 = p->v_stride[0];
+    a.vs1 = p->v_stride[1];
+    a.vs2 = p->v_stride[2];
+    a.ids = at<int32_t>(ws, L.off_ids);
+    a.counts = at<int32_t>(ws, L.off_counts);
+    a.status = const_cast<DeviceStatus *>(at<DeviceStatus>(ws, L.off_status));
+    return a;
+}
+
+TileArgs tile_args(const qsa_problem *p, const Layout &L, const void *ws) {
+    TileArgs t{};
+    t.T = L.T;
+    t.n_tiles = L.n_tiles;
+    t.max_chunks = L.max_chunks;
+    t.tile_nchunks = at<int32_t>(ws, L.off_tile_nchunks);
+    t.tile_keys = at<int32_t>(ws, L.off_tile_keys);
+    t.tile_masks = at<uint64_t>(ws, L.off_tile_masks);
+    t.order = at<int32_t>(ws, L.off_order);
+    return t;
+}
+
+}  // namespace
+}  // namespace qsa
+
+using namespace qsa;
+
+extern "C" {
+
+qsa_status qsa_check_problem(const qsa_problem *problem) { return validate(problem); }
+
+size_t qsa_workspace_bytes(const qsa_problem *problem) {
+    if (validate(problem) != QSA_OK) return 0;
+    return make_layout(problem).total;
+}
+
+qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    Layout L;
+    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    if (st != QSA_OK) return st;
+    if (!routes) return fail(QSA_ERR_INVALID_ARGUMENT, "routes is null");
+    if (reinterpret_cast<uintptr_t>(routes) % (p->route_bits / 8) != 0)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "routes pointer is not aligned to its element size");
+    cudaError_t e = cudaMemsetAsync(at<DeviceStatus>(ws, L.off_status), 0, sizeof(DeviceStatus), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    RowsArgs r{};
+    r.routes = routes;
+    r.route_bits = p->route_bits;
+    r.B = p->B;
+    r.S_q = p->S_q;
+    r.S_kv = p->S_kv;
+    r.K = p->K;
+    r.rs0 = p->r_stride[0];
+    r.rs1 = p->r_stride[1];
+    r.rs2 = p->r_stride[2];
+    r.ids = at<int32_t>(ws, L.off_ids);
+    r.counts = at<int32_t>(ws, L.off_counts);
+    e = launch_route_rows(r, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "route_rows launch");
+    if (L.T) {
+        TilesArgs t{};
+        t.B = p->B;
+        t.S_q = p->S_q;
+        t.S_kv = p->S_kv;
+        t.K = p->K;
+        t.T = L.T;
+        t.n_tiles = L.n_tiles;
+        t.max_chunks = L.max_chunks;
+        t.Hkv = p->Hkv;
+        t.ids = r.ids;
+        t.counts = r.counts;
+        t.tile_nchunks = at<int32_t>(ws, L.off_tile_nchunks);
+        t.tile_keys = at<int32_t>(ws, L.off_tile_keys);
+        t.tile_masks = at<uint64_t>(ws, L.off_tile_masks);
+        t.order = at<int32_t>(ws, L.off_order);
+        e = launch_route_tiles(t, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "route_tiles launch");
+    }
+    return QSA_OK;
+}
+
+qsa_status qsa_forward(const qsa_problem *p, const void *ws, size_t ws_bytes, const void *q, const void *k,
+                       const void *v, void *o, float *lse, cudaStream_t stream) {
+    Layout L;
+    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    if (st != QSA_OK) return st;
+    if (!q || !k || !v || !o || !lse) return fail(QSA_ERR_INVALID_ARGUMENT, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+        return fail(QSA_ERR_UNSUPPORTED, "q, k, v and o must be 16-byte aligned");
+    uintptr_t q0, q1, k0, k1, v0, v1;
+    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, q0, q1);
+    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, k0, k1);
+    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, v0, v1);
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(o), o1 = o0 + 2 * (size_t)(p->B * p->S_q * p->Hq * kHeadDim);
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(lse), l1 = l0 + 4 * (size_t)(p->B * p->Hq * p->S_q);
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(ws), w1 = w0 + L.total;
+    const uintptr_t in[4][2] = {{q0, q1}, {k0, k1}, {v0, v1}, {w0, w1}};
+    for (auto &r : in)
+        if (overlaps(o0, o1, r[0], r[1]) || overlaps(l0, l1, r[0], r[1]))
+            return fail(QSA_ERR_INVALID_ARGUMENT, "o/lse overlap an input or the workspace");
+    if (overlaps(o0, o1, l0, l1)) return fail(QSA_ERR_INVALID_ARGUMENT, "o and lse overlap");
+    AttnArgs a = attn_args(p, L, ws, q, k, v);
+    cudaError_t e;
+    if (L.T == kTileRows / 8 && tc_forward_supported()) {
+        e = launch_tc_forward(a, tile_args(p, L, ws), static_cast<__nv_bfloat16 *>(o), lse, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tile forward launch");
+    } else {
+        e = launch_rowwise_forward(a, static_cast<__nv_bfloat16 *>(o), lse, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "rowwise forward launch");
+    }
+    return QSA_OK;
+}
+
+qsa_status qsa_backward(const qsa_problem *p, void *ws, size_t ws_bytes, const void *q, const void *k, const void *v,
+                        const void *o, const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                        float *dk_f32, float *dv_f32, cudaStream_t stream) {
+    Layout L;
+    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    if (st != QSA_OK) return st;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "null tensor pointer");
+    if ((dk_f32 == nullptr) != (dv_f32 == nullptr))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "dk_f32 and dv_f32 must both be given or both be null");
+    const void *al[] = {q, k, v, o, dout, dq, dk, dv};
+    for (const void *x : al)
+        if (!aligned16(x)) return fail(QSA_ERR_UNSUPPORTED, "bf16 tensors must be 16-byte aligned");
+    if ((dk_f32 && !aligned16(dk_f32)) || (dv_f32 && !aligned16(dv_f32)))
+        return fail(QSA_ERR_UNSUPPORTED, "fp32 accumulators must be 16-byte aligned");
+    uintptr_t q0, q1, k0, k1, v0, v1;
+    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, q0, q1);
+    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, k0, k1);
+    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, v0, v1);
+    const size_t nq = 2 * (size_t)(p->B * p->S_q * p->Hq * kHeadDim);
+    const size_t nkv = 2 * (size_t)(p->B * p->S_kv * p->Hkv * kHeadDim);
+    auto u = [](const void *x) { return reinterpret_cast<uintptr_t>(x); };
+    const uintptr_t ins[6][2] = {{q0, q1}, {k0, k1}, {v0, v1}, {u(o), u(o) + nq}, {u(dout), u(dout) + nq},
+                                 {u(lse), u(lse) + 4 * (size_t)(p->B * p->Hq * p->S_q)}};
+    uintptr_t outs[5][2] = {{u(dq), u(dq) + nq}, {u(dk), u(dk) + nkv}, {u(dv), u(dv) + nkv}, {0, 0}, {0, 0}};
+    int nout = 3;
+    if (dk_f32) {
+        outs[3][0] = u(dk_f32);
+        outs[3][1] = u(dk_f32) + 2 * nkv;
+        outs[4][0] = u(dv_f32);
+        outs[4][1] = u(dv_f32) + 2 * nkv;
+        nout = 5;
+    }
+    const uintptr_t w0 = u(ws), w1 = w0 + L.total;
+    for (int i = 0; i < nout; ++i) {
+        for (auto &r : ins)
+            if (overlaps(outs[i][0], outs[i][1], r[0], r[1]))
+                return fail(QSA_ERR_INVALID_ARGUMENT, "a gradient output overlaps an input");
+        if (overlaps(outs[i][0], outs[i][1], w0, w1))
+            return fail(QSA_ERR_INVALID_ARGUMENT, "a gradient output overlaps the workspace");
+        for (int j = 0; j < i; ++j)
+            if (overlaps(outs[i][0], outs[i][1], outs[j][0], outs[j][1]))
+                return fail(QSA_ERR_INVALID_ARGUMENT, "gradient outputs overlap each other");
+    }
+    BwdArgs b{};
+    b.f = attn_args(p, L, ws, q, k, v);
+    b.o = static_cast<const __nv_bfloat16 *>(o);
+    b.dout = static_cast<const __nv_bfloat16 *>(dout);
+    b.lse = lse;
+    b.delta = at<float>(ws, L.off_delta);
+    b.dq = static_cast<__nv_bfloat16 *>(dq);
+    b.dk = static_cast<__nv_bfloat16 *>(dk);
+    b.dv = static_cast<__nv_bfloat16 *>(dv);
+    b.dk_acc = dk_f32 ? dk_f32 : at<float>(ws, L.off_dk);
+    b.dv_acc = dv_f32 ? dv_f32 : at<float>(ws, L.off_dv);
+    const size_t kv_f32 = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * sizeof(float);
+    cudaError_t e = cudaMemsetAsync(b.dk_acc, 0, kv_f32, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(b.dv_acc, 0, kv_f32, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the dK/dV accumulators");
+    e = launch_delta(b, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "delta launch");
+    if (L.T == kTileRows / 8 && tc_backward_supported()) {
+        e = launch_tc_backward(b, tile_args(p, L, ws), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
+    } else {
+        e = launch_rowwise_backward(b, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "rowwise backward launch");
+    }
+    e = launch_convert_dkdv(b, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dK/dV conversion launch");
+    return QSA_OK;
+}
+
+qsa_status qsa_copy_route_sets(const qsa_problem *p, const void *ws, size_t ws_bytes, int32_t *ids, int32_t *counts,
+                               cudaStream_t stream) {
+    Layout L;
+    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    if (st != QSA_OK) return st;
+    const size_t rows = (size_t)(p->B * p->S_q);
+    cudaError_t e = cudaSuccess;
+    if (ids)
+        e = cudaMemcpyAsync(ids, at<int32_t>(ws, L.off_ids), rows * p->K * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                            stream);
+    if (e == cudaSuccess && counts)
+        e = cudaMemcpyAsync(counts, at<int32_t>(ws, L.off_counts), rows * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                            stream);
+    if (e != cudaSuccess) return cuda_fail(e, "copying route sets");
+    return QSA_OK;
+}
+
+qsa_status qsa_read_device_status(const void *ws, cudaStream_t stream) {
+    if (!ws) return fail(QSA_ERR_INVALID_ARGUMENT, "workspace is null");
+    DeviceStatus h{};
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemsetAsync(const_cast<void *>(ws), 0, sizeof(h), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    if (h.code == 0) return QSA_OK;
+    return fail((qsa_status)h.code, "device reported %s at site %u (info %u, %u)",
+                qsa_status_string((qsa_status)h.code), h.where, h.info0, h.info1);
+}
+
+const char *qsa_status_string(qsa_status s) {
+    switch (s) {
+        case QSA_OK: return "QSA_OK";
+        case QSA_ERR_INVALID_ARGUMENT: return "QSA_ERR_INVALID_ARGUMENT";
+        case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED";
+        case QSA_ERR_WORKSPACE_TOO_SMALL: return "QSA_ERR_WORKSPACE_TOO_SMALL";
+        case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+        case QSA_ERR_TIMEOUT: return "QSA_ERR_TIMEOUT";
+        case QSA_ERR_DEVICE_CHECK: return "QSA_ERR_DEVICE_CHECK";
+    }
+    return "QSA_ERR_UNKNOWN";
+}
+
+const char *qsa_last_error(void) { return g_last_error; }
+
+}  // extern "C"

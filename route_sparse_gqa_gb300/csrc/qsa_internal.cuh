@@ -1,0 +1,125 @@
+// qsa_internal.cuh -- shared definitions of the libqsa CUDA sources (not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+constexpr int kHeadDim = 256;        // fa4_sparse_gqa_attention fixes D = 256
+constexpr int kChunkKeys = 64;       // keys per gathered chunk (one tensor-core N tile)
+constexpr int kTileRows = 128;       // (query, head) rows per tile = tcgen05 M
+constexpr int kMaxRouteSlots = 16384;  // per-row sort capacity (smem bitonic sort)
+
+// Device status word kept at the start of the workspace.  Kernels only ever
+// raise it (atomicCAS from 0); qsa_read_device_status reads and clears it.
+struct DeviceStatus {
+    unsigned int code;       // 0 = ok, else a qsa_status value
+    unsigned int where;      // kernel-specific site id of the first failure
+    unsigned int info0, info1;
+};
+
+// Workspace layout for one problem.  All offsets are 256-byte aligned.
+struct Layout {
+    int64_t G;           // query heads per KV head
+    int64_t T;           // queries per tile (kTileRows / G), 0 when the tile path does not apply
+    int64_t n_tiles;     // query tiles per batch row
+    int64_t max_chunks;  // capacity of one tile's chunk list
+    size_t off_status, off_counts, off_ids, off_tile_nchunks, off_tile_keys, off_tile_masks, off_order;
+    size_t off_delta, off_dk, off_dv, total;
+};
+
+// Device-side failure sites (DeviceStatus::where).
+enum Site : unsigned int {
+    kSiteNone = 0,
+    kSiteRowwiseFwdId = 1,
+    kSiteRowwiseBwdId = 2,
+    kSiteTileFwdWait = 10,
+    kSiteTileFwdKey = 11,
+    kSiteTileBwdWait = 20,
+    kSiteTileBwdKey = 21,
+};
+
+__device__ __forceinline__ void raise_status(DeviceStatus *st, unsigned int code, unsigned int where,
+                                             unsigned int i0 = 0, unsigned int i1 = 0) {
+    if (atomicCAS(&st->code, 0u, code) == 0u) {
+        st->where = where;
+        st->info0 = i0;
+        st->info1 = i1;
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float f[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 f32x8_to_bf16(const float f[8]) {
+    uint4 u;
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return u;
+}
+
+// ---- launch wrappers implemented in the .cu files (return cudaGetLastError()) ----
+
+struct RowsArgs {
+    const void *routes;
+    int32_t route_bits;
+    int64_t B, S_q, S_kv, K;
+    int64_t rs0, rs1, rs2;
+    int32_t *ids;     // [B*S_q, K]
+    int32_t *counts;  // [B*S_q]
+};
+cudaError_t launch_route_rows(const RowsArgs &a, cudaStream_t s);
+
+struct TilesArgs {
+    int64_t B, S_q, S_kv, K, T, n_tiles, max_chunks, Hkv;
+    const int32_t *ids;
+    const int32_t *counts;
+    int32_t *tile_nchunks;    // [B*n_tiles]
+    int32_t *tile_keys;       // [B*n_tiles, max_chunks*64]
+    uint64_t *tile_masks;     // [B*n_tiles, max_chunks, T]
+    int32_t *order;           // [B*n_tiles*Hkv] work items, heaviest first
+};
+cudaError_t launch_route_tiles(const TilesArgs &a, cudaStream_t s);
+
+struct AttnArgs {
+    int64_t B, S_q, S_kv, Hq, Hkv, K, G;
+    float scale;
+    const __nv_bfloat16 *q, *k, *v;
+    int64_t qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2;
+    const int32_t *ids, *counts;
+    DeviceStatus *status;
+};
+
+cudaError_t launch_rowwise_forward(const AttnArgs &a, __nv_bfloat16 *o, float *lse, cudaStream_t s);
+
+struct BwdArgs {
+    AttnArgs f;
+    const __nv_bfloat16 *o, *dout;
+    const float *lse;
+    float *delta;  // [B, Hq, S_q]
+    __nv_bfloat16 *dq, *dk, *dv;
+    float *dk_acc, *dv_acc;  // fp32 [B, S_kv, Hkv, D]
+};
+cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_delta(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s);
+
+}  // namespace qsa

@@ -1,0 +1,274 @@
+// qsa_preprocess.cu -- route preprocessing kernels.
+//
+// The pages' preprocessing (fa4_qsa _preprocess, _block_kinds, _compact_blocks;
+// flex_qsa _routes_to_membership) turns routes into a dense membership table and
+// block lists.  Here nothing dense is ever built in HBM:
+//
+//   route_rows_kernel  one CTA per query row: read the row's K route slots in
+//                      their own width (int32 or int64), keep 0 <= id < S_kv
+//                      (invalid values, huge int64 included, never reach an
+//                      index), bitonic-sort in shared memory, drop repeats.
+//                      Output: ascending unique IDs (int32, -1 tail) + count.
+//   route_tiles_kernel one CTA per tile of T consecutive query rows: the union
+//                      of the rows' ID sets, ascending, cut into chunks of 64
+//                      keys, and for every (chunk, query) a 64-bit mask of the
+//                      chunk keys that query routes to.  The union is built a
+//                      window of key space at a time in a shared-memory table
+//                      of per-key query bitmasks (the membership table, but
+//                      only T x W bits of it, never in HBM).
+//   route_order_kernel counting sort of tiles by chunk count, heaviest first,
+//                      for the attention kernels' static schedule.
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kRowThreads = 256;
+constexpr int kTileThreads = 256;
+constexpr int kTileWindow = 4096;  // keys per window of the shared-memory membership table
+
+__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nwarps ? warp_tot[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < nwarps) warp_tot[lane] = wi - w;  // exclusive per-warp offsets
+        if (lane == 31) warp_tot[32] = wi;
+    }
+    __syncthreads();
+    total = warp_tot[32];
+    int r = warp_tot[warp] + incl - x;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kRowThreads) route_rows_kernel(RowsArgs a, int P) {
+    extern __shared__ int32_t srt[];  // [P]
+    __shared__ int warp_tot[33];
+    const int64_t row = blockIdx.x;
+    const int64_t b = row / a.S_q, q = row % a.S_q;
+    const int tid = threadIdx.x;
+    // Validate in the route's own width before narrowing (fa4_qsa _preprocess).
+    for (int i = tid; i < P; i += blockDim.x) {
+        int32_t v = INT32_MAX;
+        if (i < a.K) {
+            const int64_t off = b * a.rs0 + q * a.rs1 + (int64_t)i * a.rs2;
+            const int64_t x = a.route_bits == 64 ? static_cast<const int64_t *>(a.routes)[off]
+                                                 : (int64_t) static_cast<const int32_t *>(a.routes)[off];
+            if (x >= 0 && x < a.S_kv) v = (int32_t)x;
+        }
+        srt[i] = v;
+    }
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = tid; i < P; i += blockDim.x) {
+                const int ixj = i ^ j;
+                if (ixj > i) {
+                    const int32_t x = srt[i], y = srt[ixj];
+                    if ((x > y) == ((i & k) == 0)) {
+                        srt[i] = y;
+                        srt[ixj] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    const int seg = (P + blockDim.x - 1) / blockDim.x;
+    const int s0 = min(P, tid * seg), s1 = min(P, s0 + seg);
+    int local = 0;
+    for (int i = s0; i < s1; ++i) local += srt[i] != INT32_MAX && (i == 0 || srt[i] != srt[i - 1]);
+    int total;
+    int pos = block_exclusive_scan(local, warp_tot, total);
+    int32_t *out = a.ids + row * a.K;
+    for (int i = s0; i < s1; ++i)
+        if (srt[i] != INT32_MAX && (i == 0 || srt[i] != srt[i - 1])) out[pos++] = srt[i];
+    for (int64_t i = total + tid; i < a.K; i += blockDim.x) out[i] = -1;
+    if (tid == 0) a.counts[row] = total;
+}
+
+// Emit one chunk of 64 union keys: keys, and for each tile query the mask of
+// the chunk's keys it routes to.  Executed by one full warp.
+__device__ __forceinline__ void emit_chunk(const TilesArgs &a, int64_t tile, int64_t chunk, const uint32_t *cw,
+                                           const int32_t *ck) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t w_lo = cw[lane], w_hi = cw[32 + lane];
+    int32_t *keys = a.tile_keys + (tile * a.max_chunks + chunk) * kChunkKeys;
+    keys[lane] = ck[lane];
+    keys[32 + lane] = ck[32 + lane];
+    uint64_t mine = 0;
+    for (int qi = 0; qi < a.T; ++qi) {
+        const uint32_t lo = __ballot_sync(0xffffffffu, (w_lo >> qi) & 1u);
+        const uint32_t hi = __ballot_sync(0xffffffffu, (w_hi >> qi) & 1u);
+        if (lane == qi) mine = (uint64_t)lo | ((uint64_t)hi << 32);
+    }
+    if (lane < a.T) a.tile_masks[(tile * a.max_chunks + chunk) * a.T + lane] = mine;
+}
+
+__global__ void __launch_bounds__(kTileThreads) route_tiles_kernel(TilesArgs a) {
+    extern __shared__ uint32_t tsm[];
+    uint32_t *mem = tsm;                                              // [W] per-key query bitmask
+    uint32_t *cw = mem + kTileWindow;                                 // [W + 64] compacted bitmasks
+    int32_t *ck = reinterpret_cast<int32_t *>(cw + kTileWindow + 64);  // [W + 64] compacted keys
+    __shared__ int ptr[32], cnt[32], warp_tot[33];
+    __shared__ int64_t s_next;
+    const int64_t tile = blockIdx.x;
+    const int64_t b = tile / a.n_tiles, t = tile % a.n_tiles;
+    const int64_t q0 = t * a.T;
+    const int nq = (int)(a.T < a.S_q - q0 ? a.T : a.S_q - q0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    if (tid < 32) {
+        ptr[tid] = 0;
+        cnt[tid] = tid < nq ? a.counts[b * a.S_q + q0 + tid] : 0;
+    }
+    __syncthreads();
+    int carry = 0;
+    int64_t nchunks = 0;
+    for (;;) {
+        if (warp == 0) {
+            int64_t nx = INT64_MAX;
+            if (lane < nq && ptr[lane] < cnt[lane]) nx = a.ids[(b * a.S_q + q0 + lane) * a.K + ptr[lane]];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) nx = min(nx, __shfl_xor_sync(0xffffffffu, nx, o));
+            if (lane == 0) s_next = nx;
+        }
+        __syncthreads();
+        const int64_t w0 = s_next;
+        if (w0 == INT64_MAX) break;
+        for (int i = tid; i < kTileWindow; i += blockDim.x) mem[i] = 0u;
+        __syncthreads();
+        for (int qi = warp; qi < nq; qi += nwarps) {
+            const int32_t *row = a.ids + (b * a.S_q + q0 + qi) * a.K;
+            int p = ptr[qi];
+            const int c = cnt[qi];
+            while (p < c) {
+                const int idx = p + lane;
+                const int64_t id = idx < c ? (int64_t)row[idx] : INT64_MAX;
+                const bool in = id < w0 + kTileWindow;
+                if (in) atomicOr(&mem[id - w0], 1u << qi);
+                const int n_in = __popc(__ballot_sync(0xffffffffu, in));
+                p += n_in;
+                if (n_in < 32) break;
+            }
+            if (lane == 0) ptr[qi] = p;
+        }
+        __syncthreads();
+        const int per = kTileWindow / kTileThreads;
+        const int base = tid * per;
+        int local = 0;
+        for (int e = 0; e < per; ++e) local += mem[base + e] != 0u;
+        int total;
+        int pos = carry + block_exclusive_scan(local, warp_tot, total);
+        for (int e = 0; e < per; ++e) {
+            const uint32_t w = mem[base + e];
+            if (w) {
+                cw[pos] = w;
+                ck[pos] = (int32_t)(w0 + base + e);
+                ++pos;
+            }
+        }
+        __syncthreads();
+        const int all = carry + total;
+        const int full = all / kChunkKeys;
+        for (int c = warp; c < full; c += nwarps) {
+            if (nchunks + c < a.max_chunks) emit_chunk(a, tile, nchunks + c, cw + c * kChunkKeys, ck + c * kChunkKeys);
+        }
+        const int rem = all - full * kChunkKeys;
+        uint32_t tw = 0;
+        int32_t tk = 0;
+        if (tid < rem) {
+            tw = cw[full * kChunkKeys + tid];
+            tk = ck[full * kChunkKeys + tid];
+        }
+        __syncthreads();
+        if (tid < rem) {
+            cw[tid] = tw;
+            ck[tid] = tk;
+        }
+        nchunks += full;
+        carry = rem;
+        __syncthreads();
+    }
+    if (carry > 0) {
+        // Last, partial chunk: pad with the chunk's first key (a valid row to
+        // gather) and an empty membership so the padding never contributes.
+        if (tid >= carry && tid < kChunkKeys) {
+            cw[tid] = 0u;
+            ck[tid] = ck[0];
+        }
+        __syncthreads();
+        if (warp == 0 && nchunks < a.max_chunks) emit_chunk(a, tile, nchunks, cw, ck);
+        ++nchunks;
+    }
+    if (tid == 0) a.tile_nchunks[tile] = (int32_t)(nchunks < a.max_chunks ? nchunks : a.max_chunks);
+}
+
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderBins = 8192;
+
+// Tiles sorted by chunk count, heaviest first (counting sort; ties in any order).
+__global__ void __launch_bounds__(kOrderThreads) route_order_kernel(const int32_t *nchunks, int64_t n, int32_t *order) {
+    __shared__ int hist[kOrderBins];
+    __shared__ int warp_tot[33];
+    for (int i = threadIdx.x; i < kOrderBins; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&hist[kOrderBins - 1 - min(nchunks[i], kOrderBins - 1)], 1);
+    __syncthreads();
+    const int per = kOrderBins / kOrderThreads;
+    int local = 0;
+    for (int e = 0; e < per; ++e) local += hist[threadIdx.x * per + e];
+    int total;
+    int pos = block_exclusive_scan(local, warp_tot, total);
+    for (int e = 0; e < per; ++e) {
+        const int h = hist[threadIdx.x * per + e];
+        hist[threadIdx.x * per + e] = pos;
+        pos += h;
+    }
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const int p = atomicAdd(&hist[kOrderBins - 1 - min(nchunks[i], kOrderBins - 1)], 1);
+        order[p] = (int32_t)i;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route_rows(const RowsArgs &a, cudaStream_t s) {
+    int P = 32;
+    while (P < a.K) P <<= 1;
+    const size_t smem = (size_t)P * sizeof(int32_t);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(route_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    route_rows_kernel<<<(unsigned)(a.B * a.S_q), kRowThreads, smem, s>>>(a, P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_tiles(const TilesArgs &a, cudaStream_t s) {
+    const size_t smem = (size_t)kTileWindow * 4 + 2 * (size_t)(kTileWindow + 64) * 4;
+    cudaError_t e = cudaFuncSetAttribute(route_tiles_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = a.B * a.n_tiles;
+    route_tiles_kernel<<<(unsigned)tiles, kTileThreads, smem, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    route_order_kernel<<<1, kOrderThreads, 0, s>>>(a.tile_nchunks, tiles, a.order);
+    return cudaGetLastError();
+}
+
+}  // namespace qsa

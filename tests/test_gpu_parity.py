@@ -1,0 +1,168 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+the same seeded inputs.  Route sets must match bit for bit; O, dQ, dK, dV within
+|gpu - ref| <= 2e-2 |ref| + 2e-2; LSE within 1e-3 absolute, -inf where the
+oracle has -inf."""
+import numpy as np
+import pytest
+
+import oracle
+from route_sparse_gqa_gb300 import workloads as W
+from tests.qsa_testlib import assert_close, assert_lse_close, f64, run_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def _full_compare(q, k, v, do, routes, scale, S_kv, fp32=False, transform=None):
+    out = run_library(q, k, v, do, routes, scale, fp32_dkdv=fp32, transform=transform)
+    ids_ref, counts_ref = oracle.route_sets(routes, S_kv)
+    assert np.array_equal(out["counts"], counts_ref)
+    assert np.array_equal(out["ids"], ids_ref)
+    qd, kd, vd, dod = f64(q), f64(k), f64(v), f64(do)
+    o_ref, lse_ref = oracle.forward(qd, kd, vd, routes, scale)
+    dq_ref, dk_ref, dv_ref = oracle.backward(qd, kd, vd, routes, dod, scale)
+    assert_close("O", out["o"], o_ref)
+    assert_lse_close(out["lse"], lse_ref)
+    assert_close("dQ", out["dq"], dq_ref)
+    assert_close("dK", out["dk"], dk_ref)
+    assert_close("dV", out["dv"], dv_ref)
+    if fp32:
+        assert_close("dK fp32", out["dk32"], dk_ref)
+        assert_close("dV fp32", out["dv32"], dv_ref)
+    return out
+
+
+def test_tiny_causal_rows_workload():
+    c = W.make_case(0)
+    w = c.workload
+    out = _full_compare(c.q, c.k, c.v, c.do, c.routes, w.softmax_scale, w.S_kv, fp32=True)
+    assert np.all(out["o"][0, 240:] == 0) and np.all(out["dq"][0, 240:] == 0)
+
+
+def _random_case(seed, B, S_q, S_kv, Hq, Hkv, K, pattern="random", dtype=np.int32, p_empty=0.1):
+    rng = np.random.default_rng(seed)
+    q = W.bf16_normal(rng, (B, S_q, Hq, 256))
+    k = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
+    v = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
+    do = W.bf16_normal(rng, (B, S_q, Hq, 256))
+    if pattern == "random":
+        routes = rng.integers(-2, S_kv + 2, size=(B, S_q, K)).astype(np.int64)
+    elif pattern == "blocks":
+        routes = np.stack([W._block_routes(rng, np.arange(S_q) % S_kv, np.zeros(S_q, np.int64), 7, K)
+                           for _ in range(B)])
+    elif pattern == "dense":  # every key, shuffled, plus padding
+        base = np.tile(np.arange(S_kv), (B, S_q, 1))
+        routes = np.concatenate([base, np.full((B, S_q, K - S_kv), -1)], axis=2)
+        routes = np.take_along_axis(routes, np.argsort(rng.random(routes.shape), axis=2), 2)
+    else:
+        raise ValueError(pattern)
+    routes[rng.random((B, S_q)) < p_empty] = -1
+    if dtype == np.int64:
+        huge = rng.random(routes.shape) < 0.05
+        routes[huge] = rng.integers(2**40, 2**62, size=huge.sum())
+        routes[rng.random(routes.shape) < 0.02] = 2**32 + 5  # would alias id 5 if narrowed first
+    return q, k, v, do, routes.astype(dtype)
+
+
+@pytest.mark.parametrize("B,S_q,S_kv,Hq,Hkv,K,pattern,dtype", [
+    (1, 100, 300, 16, 2, 50, "random", np.int32),    # G=8, ragged last tile, S_q != S_kv
+    (2, 70, 70, 8, 2, 40, "blocks", np.int64),       # G=4
+    (1, 50, 130, 32, 2, 64, "random", np.int64),     # G=16
+    (1, 33, 50, 2, 2, 20, "random", np.int32),       # G=1
+    (1, 40, 64, 12, 2, 24, "random", np.int32),      # G=6
+    (1, 64, 40, 16, 2, 48, "dense", np.int32),       # S_kv < one chunk, every key routed
+    (2, 130, 700, 16, 2, 300, "blocks", np.int32),   # several chunks per tile
+    (1, 17, 2000, 16, 2, 1, "random", np.int32),     # K = 1
+])
+def test_small_shapes(B, S_q, S_kv, Hq, Hkv, K, pattern, dtype):
+    q, k, v, do, routes = _random_case(B * 7 + S_q + K, B, S_q, S_kv, Hq, Hkv, K, pattern, dtype)
+    _full_compare(q, k, v, do, routes, 1.0 / 16, S_kv)
+
+
+def test_all_rows_empty():
+    q, k, v, do, routes = _random_case(3, 1, 40, 64, 16, 2, 8, p_empty=1.0)
+    out = _full_compare(q, k, v, do, routes, 0.1, 64)
+    assert np.all(out["o"] == 0) and np.all(np.isneginf(out["lse"]))
+    assert np.all(out["dq"] == 0) and np.all(out["dk"] == 0) and np.all(out["dv"] == 0)
+
+
+def test_strided_inputs():
+    """Q/K/V as views with non-dense strides and routes as a transposed view."""
+    import torch
+
+    q, k, v, do, routes = _random_case(11, 2, 48, 96, 16, 2, 32, "random", np.int64)
+
+    def transform(qt, kt, vt, rt):
+        qw = torch.zeros(qt.shape[0], qt.shape[1], qt.shape[2] + 8, 256, dtype=qt.dtype, device=qt.device)
+        qw[:, :, 3:3 + qt.shape[2]] = qt
+        kw = torch.zeros(kt.shape[0], kt.shape[1] * 2, kt.shape[2], 256, dtype=kt.dtype, device=kt.device)
+        kw[:, ::2] = kt
+        rT = rt.transpose(1, 2).contiguous().transpose(1, 2)
+        return qw[:, :, 3:3 + qt.shape[2]], kw[:, ::2], vt, rT
+
+    _full_compare(q, k, v, do, routes, 0.0625, 96, transform=transform)
+
+
+def test_scale_default_and_scale_changes_result():
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+    from tests.qsa_testlib import bf16_to_device
+
+    q, k, v, _, routes = _random_case(5, 1, 20, 40, 16, 2, 10)
+    dev = torch.device("cuda:0")
+    qt, kt, vt = (bf16_to_device(x, dev) for x in (q, k, v))
+    rt = torch.from_numpy(routes).to(dev)
+    o_default = qsa.qsa_attention(qt, kt, vt, rt)
+    o_16 = qsa.qsa_attention(qt, kt, vt, rt, 1.0 / 16)
+    o_1 = qsa.qsa_attention(qt, kt, vt, rt, 1.0)
+    assert torch.equal(o_default, o_16)
+    assert not torch.equal(o_default, o_1)
+
+
+def test_invalid_arguments_raise():
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    dev = torch.device("cuda:0")
+    q = torch.zeros(1, 8, 16, 256, dtype=torch.bfloat16, device=dev)
+    k = torch.zeros(1, 8, 2, 256, dtype=torch.bfloat16, device=dev)
+    r = torch.zeros(1, 8, 4, dtype=torch.int32, device=dev)
+    with pytest.raises(qsa.QSAError, match="INVALID"):
+        qsa.qsa_attention(q, k, k, r, -1.0)
+    with pytest.raises(qsa.QSAError, match="INVALID"):
+        qsa.qsa_attention(q[:, :, :15], k, k, r)  # Hq not a multiple of Hkv
+    with pytest.raises(qsa.QSAError, match="UNSUPPORTED"):
+        qsa.qsa_attention(q.float(), k, k, r)
+    with pytest.raises(qsa.QSAError, match="UNSUPPORTED"):
+        qsa.qsa_attention(q[..., :128], k[..., :128], k[..., :128], r)
+    with pytest.raises(qsa.QSAError, match="INVALID"):
+        qsa.qsa_attention(q, k, k[:, :4], r)
+
+
+def test_autograd_matches_explicit_backward():
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+    from tests.qsa_testlib import bf16_to_device
+
+    q, k, v, do, routes = _random_case(9, 1, 30, 60, 16, 2, 12)
+    dev = torch.device("cuda:0")
+    qt, kt, vt, dot = (bf16_to_device(x, dev) for x in (q, k, v, do))
+    rt = torch.from_numpy(routes).to(dev)
+    qt.requires_grad_(True), kt.requires_grad_(True), vt.requires_grad_(True)
+    o = qsa.qsa_attention(qt, kt, vt, rt)
+    o.backward(dot)
+    plan = qsa.preprocess(qt.detach(), kt.detach(), vt.detach(), rt)
+    o2, lse2 = qsa.forward(plan, qt.detach(), kt.detach(), vt.detach())
+    dq, dk, dv = qsa.backward(plan, qt.detach(), kt.detach(), vt.detach(), o2, lse2, dot)
+    assert torch.equal(o.detach(), o2)
+    for a, b in ((qt.grad, dq), (kt.grad, dk), (vt.grad, dv)):
+        assert torch.allclose(a.float(), b.float(), rtol=1e-2, atol=1e-2)
