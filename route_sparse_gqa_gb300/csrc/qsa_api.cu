@@ -248,8 +248,9 @@ qsa_status qsa_forward(const qsa_problem *p, const void *ws, size_t ws_bytes, co
     if (overlaps(o0, o1, l0, l1)) return fail(QSA_ERR_INVALID_ARGUMENT, "o and lse overlap");
     AttnArgs a = attn_args(p, L, ws, q, k, v);
     cudaError_t e;
-    if (L.T == kTileRows / 8 && tc_forward_supported()) {
-        e = launch_tc_forward(a, tile_args(p, L, ws), static_cast<__nv_bfloat16 *>(o), lse, stream);
+    const TileArgs ta = tile_args(p, L, ws);
+    if (L.T && tc_forward_supported() && tc_forward_shape_ok(a, ta)) {
+        e = launch_tc_forward(a, ta, static_cast<__nv_bfloat16 *>(o), lse, stream);
         if (e != cudaSuccess) return cuda_fail(e, "tile forward launch");
     } else {
         e = launch_rowwise_forward(a, static_cast<__nv_bfloat16 *>(o), lse, stream);

@@ -1,0 +1,543 @@
+// qsa_fwd_tc.cu -- tile forward of route-set sparse GQA on tcgen05 tensor cores.
+//
+// Work item = (KV head g, tile of T = 128/G consecutive query rows of one batch
+// row).  Its 128 (query, head) rows -- T queries x the G query heads that read
+// KV head g -- form the M = 128 rows of every MMA.  The preprocessing pass gave
+// the tile the ascending union of its rows' route sets cut into chunks of 64
+// keys, with a 64-bit membership mask per (chunk, query).  For every chunk:
+//
+//   producer warp   gathers the chunk's 64 K rows and 64 V rows of head g from
+//                   HBM/L2 with TMA tile::gather4 (four arbitrary rows per
+//                   instruction) into 128-byte-swizzled shared memory, plus
+//                   the chunk's masks (bulk copy);
+//   MMA warp        S = Q K^T (M=128, N=64, K=256) into TMEM, later
+//                   O += P V (M=128, N=256, K=64) into a TMEM accumulator;
+//   softmax warps   (4 warps, thread i owns TMEM lane / row i) read S, apply
+//                   the row's membership bits, run the online softmax in fp32
+//                   (base-2, scale folded in, lazy rescale of O when the
+//                   running max grows by more than 2^8), write P as BF16 into
+//                   shared memory for the PV MMA, and finally normalise O,
+//                   store it as BF16 and write LSE (natural log).
+//
+// Every K/V row gathered once into shared memory serves all G heads of the
+// group and all T queries of the tile that route to it.  Keys a query does not
+// route to get P = 0 exactly, so the result is the exact route-set softmax.
+//
+// Pipelining: two K/V stages, two S buffers in TMEM and two P buffers, so the
+// gather of chunk c+1 and the QK^T of chunk c+1 overlap the softmax of chunk c
+// and the PV of chunk c-1.  Every mbarrier wait is bounded in time; on timeout
+// the kernel records QSA_ERR_TIMEOUT in the workspace status word, all roles
+// wind down, the TMEM is freed and the kernel returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "qsa_tc.cuh"
+#include "qsa_tc_ptx.cuh"
+
+namespace qsa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kStages = 2;
+constexpr int kThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kMaxPairs = 64;  // (b, g) tensor-map pairs per launch
+constexpr uint32_t kQBytes = kTileRows * kHeadDim * 2;       // 64 KiB
+constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;     // 32 KiB per K or V chunk
+constexpr uint32_t kPBytes = kTileRows * kChunkKeys * 2;     // 16 KiB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
+constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
+constexpr uint32_t kOffMask = kOffP + 2 * kPBytes;            // kStages x 256 B
+constexpr uint32_t kOffBar = kOffMask + kStages * 256;
+constexpr uint32_t kNumBars = 5 + 3 * kStages + 2 * 2;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0, kTmemS = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr float kRescaleThreshold = 8.0f;          // log2 units
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct FwdParams {
+    CUtensorMap q_map;                  // 4-D {D, Hq, S_q, B}, box {64, G, T, 1}
+    CUtensorMap kv_maps[2 * kMaxPairs];  // per (b, g): K then V, 2-D {D, S_kv}, box {64, 1}
+    int64_t B, S_q, Hq, G, T, n_tiles, max_chunks;
+    int64_t g0, n_g;   // KV heads handled by this launch
+    int64_t n_items;   // n_g * B * n_tiles
+    float sl2;         // softmax_scale * log2(e)
+    const int32_t *tile_nchunks;
+    const int32_t *tile_keys;
+    const uint64_t *tile_masks;
+    const int32_t *order;
+    __nv_bfloat16 *o;
+    float *lse;
+    DeviceStatus *status;
+};
+
+struct Item {
+    int64_t b, g, tile, t;
+    int nch;
+};
+
+__device__ __forceinline__ bool item_at(const FwdParams &p, int64_t round, Item &it) {
+    const int64_t grid = gridDim.x;
+    const int64_t idx = round * grid + ((round & 1) ? (grid - 1 - blockIdx.x) : blockIdx.x);  // snake order
+    if (idx >= p.n_items) return false;
+    const int64_t per_g = p.B * p.n_tiles;
+    it.g = p.g0 + idx / per_g;
+    it.tile = p.order[idx % per_g];
+    it.b = it.tile / p.n_tiles;
+    it.t = it.tile % p.n_tiles;
+    it.nch = p.tile_nchunks[it.tile];
+    return true;
+}
+
+struct Bars {
+    uint64_t *q_full, *q_empty, *o_ready, *o_free, *drain;
+    uint64_t *k_full, *v_full, *kv_empty;  // [kStages]
+    uint64_t *s_full, *p_full;             // [2]
+};
+
+__device__ __forceinline__ Bars bars_at(uint8_t *smem) {
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    Bars r;
+    r.q_full = b + 0;
+    r.q_empty = b + 1;
+    r.o_ready = b + 2;
+    r.o_free = b + 3;
+    r.drain = b + 4;
+    r.k_full = b + 5;
+    r.v_full = b + 5 + kStages;
+    r.kv_empty = b + 5 + 2 * kStages;
+    r.s_full = b + 5 + 3 * kStages;
+    r.p_full = b + 5 + 3 * kStages + 2;
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const Bars bar = bars_at(smem);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar.q_full, 1);
+        mbar_init(bar.q_empty, 1);
+        mbar_init(bar.o_ready, 1);
+        mbar_init(bar.o_free, 128);
+        mbar_init(bar.drain, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar.k_full + s, 1);
+            mbar_init(bar.v_full + s, 1);
+            mbar_init(bar.kv_empty + s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar.s_full + s, 1);
+            mbar_init(bar.p_full + s, 128);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&p.q_map);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&](unsigned where, unsigned info) {
+        raise_status(p.status, QSA_ERR_TIMEOUT, where, info, blockIdx.x);
+        *abort_flag = 1;
+    };
+
+    if (warp == 4) {
+        // ---------------- producer ----------------
+        int64_t gc = 0, qc = 0;
+        int64_t last_gc[kStages];
+        for (int i = 0; i < kStages; ++i) last_gc[i] = -1;
+        Item it;
+        for (int64_t round = 0; item_at(p, round, it) && !*abort_flag; ++round) {
+            if (it.nch == 0) continue;
+            if (qc > 0 && !mbar_wait(bar.q_empty, (qc - 1) & 1, abort_flag, kWaitLimitNs)) {
+                if (lane == 0) fail(kSiteTileFwdWait, 1);
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar.q_full, kQBytes);
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_load_4d(sbase + kOffQ + kb * (kQBytes / 4), &p.q_map, bar.q_full, kb * 64, (int)(it.g * p.G),
+                                (int)(it.t * p.T), (int)it.b);
+            }
+            ++qc;  // Q loads issued so far
+            const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
+            const CUtensorMap *kmap = &p.kv_maps[2 * pair], *vmap = &p.kv_maps[2 * pair + 1];
+            const int32_t *keys = p.tile_keys + it.tile * p.max_chunks * kChunkKeys;
+            const uint64_t *masks = p.tile_masks + it.tile * p.max_chunks * p.T;
+            bool ok = true;
+            for (int c = 0; c < it.nch; ++c, ++gc) {
+                const int s = (int)(gc % kStages);
+                if (gc >= kStages && !mbar_wait(bar.kv_empty + s, ((gc / kStages) - 1) & 1, abort_flag, kWaitLimitNs)) {
+                    if (lane == 0) fail(kSiteTileFwdWait, 2);
+                    ok = false;
+                    break;
+                }
+                int4 kk = make_int4(0, 0, 0, 0);
+                if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar.k_full + s, kKVBytes + (uint32_t)(p.T * 8));
+                    bulk_load(sbase + kOffMask + s * 256, masks + c * p.T, (uint32_t)(p.T * 8), bar.k_full + s);
+                }
+                __syncwarp();
+                if (lane < 16) {
+                    const uint32_t dst = sbase + kOffK + s * kKVBytes + lane * 512;
+                    for (int kb = 0; kb < 4; ++kb)
+                        tma_gather4(dst + kb * (kKVBytes / 4), kmap, bar.k_full + s, kb * 64, kk.x, kk.y, kk.z, kk.w);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(bar.v_full + s, kKVBytes);
+                __syncwarp();
+                if (lane < 16) {
+                    const uint32_t dst = sbase + kOffV + s * kKVBytes + lane * 512;
+                    for (int kb = 0; kb < 4; ++kb)
+                        tma_gather4(dst + kb * (kKVBytes / 4), vmap, bar.v_full + s, kb * 64, kk.x, kk.y, kk.z, kk.w);
+                }
+                __syncwarp();
+                last_gc[s] = gc;
+            }
+            if (!ok) break;
+        }
+        // Drain: every issued copy must have landed before the CTA leaves.
+        if (lane == 0) {
+            const int zero = 0;
+            bool drained = true;
+            for (int i = 0; i < kStages; ++i)
+                if (last_gc[i] >= 0) {
+                    const uint32_t par = (uint32_t)((last_gc[i] / kStages) & 1);
+                    drained &= mbar_wait(bar.k_full + i, par, &zero, kWaitLimitNs);
+                    drained &= mbar_wait(bar.v_full + i, par, &zero, kWaitLimitNs);
+                }
+            if (qc > 0) drained &= mbar_wait(bar.q_full, (uint32_t)((qc - 1) & 1), &zero, kWaitLimitNs);
+            if (!drained) fail(kSiteTileFwdWait, 5);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t idesc_qk = idesc_bf16(kTileRows, kChunkKeys, false, false);
+        constexpr uint32_t idesc_pv = idesc_bf16(kTileRows, kHeadDim, false, true);
+        int64_t gc = 0, qc = 0;
+        Item it;
+        bool ok = true;
+        auto issue_pv = [&](int64_t g2, bool first) -> bool {
+            const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
+            if (!mbar_wait(bar.p_full + sb, (g2 >> 1) & 1, abort_flag, kWaitLimitNs)) return false;
+            if (!mbar_wait(bar.v_full + s, (g2 / kStages) & 1, abort_flag, kWaitLimitNs)) return false;
+            if (first && qc > 0 && !mbar_wait(bar.o_free, (qc - 1) & 1, abort_flag, kWaitLimitNs)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t pa = sbase + kOffP + sb * kPBytes;
+                const uint32_t va = sbase + kOffV + s * kKVBytes;
+#pragma unroll
+                for (int k = 0; k < kChunkKeys / 16; ++k) {
+                    const uint64_t ad = sdesc_sw128(pa + k * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(va + k * 2048, kKVBytes / 4, 1024);
+                    mma_bf16(tmem + kTmemO, ad, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+                }
+                mma_commit(bar.kv_empty + s);
+                mma_commit(bar.o_ready);
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+            if (it.nch == 0) continue;
+            if (!mbar_wait(bar.q_full, qc & 1, abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int c = 0; c < it.nch; ++c, ++gc) {
+                const int s = (int)(gc % kStages), sb = (int)(gc & 1);
+                if (!mbar_wait(bar.k_full + s, (gc / kStages) & 1, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + s * kKVBytes;
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t ad = sdesc_sw128(qa + kb * (kQBytes / 4) + k * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(ka + kb * (kKVBytes / 4) + k * 32, 16, 1024);
+                            mma_bf16(tmem + kTmemS + sb * kChunkKeys, ad, bd, idesc_qk, (kb | k) ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(bar.s_full + sb);
+                }
+                __syncwarp();
+                if (c > 0 && !issue_pv(gc - 1, c == 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (!ok) break;
+            if (!issue_pv(gc - 1, it.nch == 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mma_commit(bar.q_empty);
+            __syncwarp();
+            ++qc;
+        }
+        if (!ok && lane == 0) fail(kSiteTileFwdWait, 3);
+        // Drain: all issued MMAs complete before the TMEM is released.
+        if (lane == 0) {
+            const int zero = 0;
+            mma_commit(bar.drain);
+            if (!mbar_wait(bar.drain, 0, &zero, kWaitLimitNs)) fail(kSiteTileFwdWait, 6);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax / epilogue (warps 0-3) ----------------
+        const int r = threadIdx.x;  // row of the tile = TMEM lane
+        const int qi = (int)(r / p.G), hl = (int)(r % p.G);
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        int64_t gc = 0, qc = 0;
+        Item it;
+        bool ok = true;
+        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+            const int64_t q = it.t * p.T + qi;
+            const int64_t h = it.g * p.G + hl;
+            const bool live = q < p.S_q;
+            __nv_bfloat16 *orow = p.o + ((it.b * p.S_q + q) * p.Hq + h) * kHeadDim;
+            if (it.nch == 0) {
+                if (live) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < kHeadDim / 8; ++i) reinterpret_cast<uint4 *>(orow)[i] = z;
+                    p.lse[(it.b * p.Hq + h) * p.S_q + q] = -INFINITY;
+                }
+                continue;
+            }
+            float m = -INFINITY, l = 0.f;
+            for (int c = 0; c < it.nch; ++c, ++gc) {
+                const int s = (int)(gc % kStages), sb = (int)(gc & 1);
+                if (!mbar_wait(bar.s_full + sb, (gc >> 1) & 1, abort_flag, kWaitLimitNs) ||
+                    !mbar_wait(bar.k_full + s, (gc / kStages) & 1, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t mask = reinterpret_cast<const uint64_t *>(smem + kOffMask + s * 256)[qi];
+                uint32_t sr[2][32];
+                tmem_ld32(trow + kTmemS + sb * kChunkKeys, sr[0]);
+                tmem_ld32(trow + kTmemS + sb * kChunkKeys + 32, sr[1]);
+                tmem_ld_wait();
+                float x[64];
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    x[j] = ((mask >> j) & 1ull) ? __uint_as_float(sr[j >> 5][j & 31]) * p.sl2 : -INFINITY;
+                    mx = fmaxf(mx, x[j]);
+                }
+                const bool need = (m != -INFINITY) && (mx > m + kRescaleThreshold);
+                if (m == -INFINITY) m = mx;  // first keys of this row: nothing accumulated yet
+                if (__any_sync(0xffffffffu, need)) {
+                    // Rescale O: wait until the previous chunk's PV has landed in TMEM.
+                    if (!mbar_wait(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float alpha = need ? ex2(m - mx) : 1.f;
+#pragma unroll 1
+                    for (int blk = 0; blk < kHeadDim / 32; ++blk) {
+                        uint32_t o[32];
+                        tmem_ld32(trow + kTmemO + blk * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(trow + kTmemO + blk * 32, o);
+                    }
+                    tmem_st_wait();
+                    if (need) {
+                        l *= alpha;
+                        m = mx;
+                    }
+                }
+                uint32_t pk[32];
+                float lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 64; j += 2) {
+                    const float p0 = (m == -INFINITY) ? 0.f : ex2(x[j] - m);
+                    const float p1 = (m == -INFINITY) ? 0.f : ex2(x[j + 1] - m);
+                    lsum += p0 + p1;
+                    pk[j >> 1] = pack_bf16(p0, p1);
+                }
+                l += lsum;
+                uint8_t *prow = smem + kOffP + sb * kPBytes + r * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const int phys = ch ^ (r & 7);
+                    *reinterpret_cast<uint4 *>(prow + phys * 16) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar.p_full + sb);
+            }
+            if (!ok) break;
+            // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)).
+            if (!mbar_wait(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, kWaitLimitNs)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int blk = 0; blk < kHeadDim / 32; ++blk) {
+                uint32_t o[32];
+                tmem_ld32(trow + kTmemO + blk * 32, o);
+                tmem_ld_wait();
+                if (live) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[i + e]) * inv;
+                        reinterpret_cast<uint4 *>(orow + blk * 32 + i)[0] = f32x8_to_bf16(f);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar.o_free);
+            if (live) p.lse[(it.b * p.Hq + h) * p.S_q + q] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
+            ++qc;
+        }
+        if (!ok) fail(kSiteTileFwdWait, 4);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool encode_2d_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems) {
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_forward_supported() {
+    static int ok = -1;
+    if (ok < 0) {
+        int dev = 0, major = 0, minor = 0;
+        ok = cudaGetDevice(&dev) == cudaSuccess &&
+             cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess && major == 10 &&
+             minor == 3 && encode_fn() != nullptr;
+    }
+    return ok == 1;
+}
+
+bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t) {
+    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs;
+}
+
+cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s) {
+    FwdParams p;
+    memset(&p, 0, sizeof(p));
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.Hq, (cuuint64_t)a.S_q, (cuuint64_t)a.B};
+        const cuuint64_t strides[3] = {(cuuint64_t)a.qs2 * 2, (cuuint64_t)a.qs1 * 2, (cuuint64_t)a.qs0 * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)a.G, (cuuint32_t)t.T, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (encode_fn()(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<__nv_bfloat16 *>(a.q), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t g_per_launch = std::max<int64_t>(1, kMaxPairs / a.B);
+    p.B = a.B;
+    p.S_q = a.S_q;
+    p.Hq = a.Hq;
+    p.G = a.G;
+    p.T = t.T;
+    p.n_tiles = t.n_tiles;
+    p.max_chunks = t.max_chunks;
+    p.sl2 = a.scale * kLog2e;
+    p.tile_nchunks = t.tile_nchunks;
+    p.tile_keys = t.tile_keys;
+    p.tile_masks = t.tile_masks;
+    p.order = t.order;
+    p.o = o;
+    p.lse = lse;
+    p.status = a.status;
+    for (int64_t g0 = 0; g0 < a.Hkv; g0 += g_per_launch) {
+        const int64_t n_g = std::min<int64_t>(g_per_launch, a.Hkv - g0);
+        p.g0 = g0;
+        p.n_g = n_g;
+        p.n_items = n_g * a.B * t.n_tiles;
+        for (int64_t b = 0; b < a.B; ++b)
+            for (int64_t gi = 0; gi < n_g; ++gi) {
+                const int pair = (int)(b * n_g + gi);
+                const int64_t g = g0 + gi;
+                if (!encode_2d_rows(&p.kv_maps[2 * pair], a.k + b * a.ks0 + g * a.ks2, a.S_kv, a.ks1) ||
+                    !encode_2d_rows(&p.kv_maps[2 * pair + 1], a.v + b * a.vs0 + g * a.vs2, a.S_kv, a.vs1))
+                    return cudaErrorInvalidValue;
+            }
+        const int grid = (int)std::min<int64_t>(p.n_items, sms);
+        tc_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace qsa

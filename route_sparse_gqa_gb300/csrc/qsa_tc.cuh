@@ -17,6 +17,7 @@ struct TileArgs {
 };
 
 bool tc_forward_supported();
+bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t);
 cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s);
 
 bool tc_backward_supported();
