@@ -128,6 +128,23 @@ QSA_API qsa_status qsa_backward(const qsa_problem *problem, void *workspace, siz
 QSA_API qsa_status qsa_copy_route_sets(const qsa_problem *problem, const void *workspace, size_t ws_bytes, int32_t *ids,
                                int32_t *counts, cudaStream_t stream);
 
+/* Route preprocessing and forward pass in one call that allocates nothing and
+ * takes no workspace; the pages have no counterpart to it.  It is meant for
+ * callers that cannot allocate device memory while they run (code executing
+ * inside a framework that owns all device memory, such as an inference engine
+ * plugin's enqueue, or a latency-critical loop that cannot afford an
+ * allocation's implicit synchronisation).  Instead of a caller workspace it
+ * uses one fixed 32 MiB device array inside the library, which every GPU that
+ * loads it keeps until the process exits; problems whose
+ * qsa_workspace_bytes() exceeds 32 MiB are rejected with QSA_ERR_UNSUPPORTED.
+ * The first call on a device looks up that array's device address (with the
+ * device current), so make that first call before any stream capture.  All
+ * calls share the one array and it keeps the last call's contents: calls that
+ * overlap on the GPU (other streams, other host threads) race with each other.
+ * Outputs and conventions are those of qsa_preprocess + qsa_forward. */
+QSA_API qsa_status qsa_forward_no_alloc(const qsa_problem *problem, const void *routes, const void *q, const void *k,
+                                        const void *v, void *o, float *lse, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the workspace's device status
  * word: QSA_ERR_TIMEOUT if a kernel's bounded wait gave up, QSA_ERR_DEVICE_CHECK
  * if a device bounds check fired, QSA_OK otherwise.  Blocks the host. */

@@ -28,6 +28,7 @@ EXPORTS = (
     "qsa_forward",
     "qsa_backward",
     "qsa_copy_route_sets",
+    "qsa_forward_no_alloc",
     "qsa_read_device_status",
     "qsa_status_string",
     "qsa_last_error",
@@ -74,13 +75,14 @@ def load() -> ctypes.CDLL:
         lib.qsa_forward.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp]
         lib.qsa_backward.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_copy_route_sets.argtypes = [P, vp, sz, vp, vp, vp]
+        lib.qsa_forward_no_alloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_read_device_status.argtypes = [vp, vp]
         lib.qsa_status_string.argtypes = [ctypes.c_int]
         lib.qsa_status_string.restype = ctypes.c_char_p
         lib.qsa_last_error.argtypes = []
         lib.qsa_last_error.restype = ctypes.c_char_p
         for name in ("qsa_check_problem", "qsa_preprocess", "qsa_forward", "qsa_backward", "qsa_copy_route_sets",
-                     "qsa_read_device_status"):
+                     "qsa_forward_no_alloc", "qsa_read_device_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

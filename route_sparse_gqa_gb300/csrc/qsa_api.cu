@@ -168,6 +168,9 @@ TileArgs tile_args(const qsa_problem *p, const Layout &L, const void *ws) {
 }
 
 }  // namespace
+
+qsa_status report_error(qsa_status st, const char *msg) { return fail(st, "%s", msg); }
+
 }  // namespace qsa
 
 using namespace qsa;

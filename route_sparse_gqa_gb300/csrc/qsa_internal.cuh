@@ -76,6 +76,9 @@ __device__ __forceinline__ uint4 f32x8_to_bf16(const float f[8]) {
     return u;
 }
 
+// Records `msg` as the calling thread's qsa_last_error() and returns `st`.
+qsa_status report_error(qsa_status st, const char *msg);
+
 // ---- launch wrappers implemented in the .cu files (return cudaGetLastError()) ----
 
 struct RowsArgs {
