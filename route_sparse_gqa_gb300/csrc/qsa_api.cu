@@ -323,8 +323,9 @@ qsa_status qsa_backward(const qsa_problem *p, void *ws, size_t ws_bytes, const v
     if (e != cudaSuccess) return cuda_fail(e, "clearing the dK/dV accumulators");
     e = launch_delta(b, stream);
     if (e != cudaSuccess) return cuda_fail(e, "delta launch");
-    if (L.T == kTileRows / 8 && tc_backward_supported()) {
-        e = launch_tc_backward(b, tile_args(p, L, ws), stream);
+    const TileArgs ta = tile_args(p, L, ws);
+    if (L.T && tc_backward_supported() && tc_backward_shape_ok(b.f, ta)) {
+        e = launch_tc_backward(b, ta, stream);
         if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
     } else {
         e = launch_rowwise_backward(b, stream);

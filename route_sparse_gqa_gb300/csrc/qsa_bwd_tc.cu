@@ -1,0 +1,509 @@
+// qsa_bwd_tc.cu -- tile backward of route-set sparse GQA on tcgen05 tensor cores.
+//
+// Same work items as the tile forward: (KV head g, tile of T = 128/G query
+// rows); the tile's 128 (query, head) rows are the MMA M.  P is recomputed from
+// the forward's LSE (P_j = exp(s_j - LSE)); Delta = <dO, O> per row comes from
+// a small kernel beforehand.  Per 64-key chunk of the tile's routed-key union:
+//
+//   producer warp  gathers V then K rows (TMA tile::gather4) once the previous
+//                  chunk's MMAs have released them (single stage each; V is
+//                  free early, after the dP MMA);
+//   MMA warp       S = Q K^T and dP = dO V^T (M128 N64 K256) into TMEM;
+//                  after the softmax: dQ += dS K (M128 N256 K64, TMEM
+//                  accumulator over all chunks of the item), then for each
+//                  half of D: dK^T = Q^T dS and dV^T = dO^T P (M128 N64 K128,
+//                  both operands MN-major straight from the Q/dO tiles and the
+//                  P/dS buffers) into TMEM;
+//   softmax warps  thread = row: P = mask ? exp2(s*scale*log2e - LSE*log2e) : 0,
+//                  dS = scale * P * (dP - Delta), both written as BF16 into
+//                  swizzled shared memory; at the end of the item read dQ from
+//                  TMEM and store it (BF16);
+//   flush warps    thread = one head-dimension index: read a half's dK^T and
+//                  dV^T columns (one per chunk key) from TMEM and scatter-add
+//                  them into the fp32 dK/dV accumulators -- one coalesced
+//                  128-byte reduction per warp, key and matrix.
+//
+// So each gathered K/V row and each (key, d) accumulator update serves every
+// head of the group and every tile query that routes to that key, instead of
+// once per (query, head).  TMEM (512 columns): dQ 0-255, S 256-319,
+// dP 320-383, dK^T 384-447, dV^T 448-511.  All waits are bounded (2 s); a
+// timeout is recorded in the status word, the roles wind down, in-flight
+// copies and MMAs are drained, and the TMEM is freed.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "qsa_tc.cuh"
+#include "qsa_tc_ptx.cuh"
+
+namespace qsa {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 320;  // warps 0-3 softmax, 4-7 flush, 8 producer, 9 MMA
+constexpr int kMaxPairs = 64;
+constexpr uint32_t kTileBytes = kTileRows * kHeadDim * 2;    // 64 KiB (Q or dO tile)
+constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;     // 32 KiB
+constexpr uint32_t kPBytes = kTileRows * kChunkKeys * 2;     // 16 KiB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffDO = kOffQ + kTileBytes;
+constexpr uint32_t kOffK = kOffDO + kTileBytes;
+constexpr uint32_t kOffV = kOffK + kKVBytes;
+constexpr uint32_t kOffP = kOffV + kKVBytes;
+constexpr uint32_t kOffDS = kOffP + kPBytes;
+constexpr uint32_t kOffBar = kOffDS + kPBytes;
+constexpr uint32_t kNumBars = 16;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemDQ = 0, kTmemS = 256, kTmemDP = 320, kTmemDKT = 384, kTmemDVT = 448;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+    CUtensorMap q_map, do_map;          // 4-D {D, Hq, S_q, B}, box {64, G, T, 1}
+    CUtensorMap kv_maps[2 * kMaxPairs];  // per (b, g): K then V rows
+    int64_t B, S_q, S_kv, Hq, Hkv, G, T, n_tiles, max_chunks;
+    int64_t g0, n_g, n_items;
+    float sl2, scale;
+    const int32_t *tile_nchunks;
+    const int32_t *tile_keys;
+    const uint64_t *tile_masks;
+    const int32_t *order;
+    const float *lse, *delta;
+    __nv_bfloat16 *dq;
+    float *dk_acc, *dv_acc;
+    DeviceStatus *status;
+};
+
+struct Item {
+    int64_t b, g, tile, t;
+    int nch;
+};
+
+__device__ __forceinline__ bool item_at(const BwdParams &p, int64_t round, Item &it) {
+    const int64_t grid = gridDim.x;
+    const int64_t idx = round * grid + ((round & 1) ? (grid - 1 - blockIdx.x) : blockIdx.x);
+    if (idx >= p.n_items) return false;
+    const int64_t per_g = p.B * p.n_tiles;
+    it.g = p.g0 + idx / per_g;
+    it.tile = p.order[idx % per_g];
+    it.b = it.tile / p.n_tiles;
+    it.t = it.tile % p.n_tiles;
+    it.nch = p.tile_nchunks[it.tile];
+    return true;
+}
+
+enum BarId {
+    kQFull, kQEmpty, kKFull, kKEmpty, kVFull, kVEmpty, kSDFull, kPDSFull, kPDSEmpty, kGradsFull, kFlushDone,
+    kDQReady, kDQFree, kDrain
+};
+
+__global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        const uint32_t counts[kDrain + 1] = {1, 1, 1, 1, 1, 1, 1, 128, 1, 1, 128, 1, 128, 1};
+        for (int i = 0; i <= kDrain; ++i) mbar_init(bars + i, counts[i]);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        prefetch_tmap(&p.q_map);
+        prefetch_tmap(&p.do_map);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int zero = 0;
+
+    auto fail = [&](unsigned info) {
+        raise_status(p.status, QSA_ERR_TIMEOUT, kSiteTileBwdWait, info, blockIdx.x);
+        *abort_flag = 1;
+    };
+    auto wait = [&](int id, int64_t phase) { return mbar_wait(bars + id, (uint32_t)(phase & 1), abort_flag, kWaitLimitNs); };
+
+    if (warp == 8) {
+        // ---------------- producer ----------------
+        int64_t gc = 0, qc = 0;
+        Item it;
+        bool ok = true;
+        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+            if (it.nch == 0) continue;
+            if (qc > 0 && !wait(kQEmpty, qc - 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bars + kQFull, 2 * kTileBytes);
+                for (int kb = 0; kb < 4; ++kb) {
+                    tma_load_4d(sbase + kOffQ + kb * (kTileBytes / 4), &p.q_map, bars + kQFull, kb * 64,
+                                (int)(it.g * p.G), (int)(it.t * p.T), (int)it.b);
+                    tma_load_4d(sbase + kOffDO + kb * (kTileBytes / 4), &p.do_map, bars + kQFull, kb * 64,
+                                (int)(it.g * p.G), (int)(it.t * p.T), (int)it.b);
+                }
+            }
+            ++qc;
+            const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
+            const CUtensorMap *kmap = &p.kv_maps[2 * pair], *vmap = &p.kv_maps[2 * pair + 1];
+            const int32_t *keys = p.tile_keys + it.tile * p.max_chunks * kChunkKeys;
+            for (int c = 0; c < it.nch; ++c, ++gc) {
+                int4 kk = make_int4(0, 0, 0, 0);
+                if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
+                if (gc > 0 && !wait(kVEmpty, gc - 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(bars + kVFull, kKVBytes);
+                __syncwarp();
+                if (lane < 16) {
+                    const uint32_t dst = sbase + kOffV + lane * 512;
+                    for (int kb = 0; kb < 4; ++kb)
+                        tma_gather4(dst + kb * (kKVBytes / 4), vmap, bars + kVFull, kb * 64, kk.x, kk.y, kk.z, kk.w);
+                }
+                __syncwarp();
+                if (gc > 0 && !wait(kKEmpty, gc - 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(bars + kKFull, kKVBytes);
+                __syncwarp();
+                if (lane < 16) {
+                    const uint32_t dst = sbase + kOffK + lane * 512;
+                    for (int kb = 0; kb < 4; ++kb)
+                        tma_gather4(dst + kb * (kKVBytes / 4), kmap, bars + kKFull, kb * 64, kk.x, kk.y, kk.z, kk.w);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) fail(1);
+        // Drain every issued copy before the CTA can leave.
+        if (lane == 0) {
+            bool drained = true;
+            if (gc > 0) {
+                drained &= mbar_wait(bars + kVFull, (uint32_t)((gc - 1) & 1), &zero, kWaitLimitNs);
+                drained &= mbar_wait(bars + kKFull, (uint32_t)((gc - 1) & 1), &zero, kWaitLimitNs);
+            }
+            if (qc > 0) drained &= mbar_wait(bars + kQFull, (uint32_t)((qc - 1) & 1), &zero, kWaitLimitNs);
+            if (!drained) fail(2);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t idesc_n64 = idesc_bf16(kTileRows, kChunkKeys, false, false);   // S, dP
+        constexpr uint32_t idesc_dq = idesc_bf16(kTileRows, kHeadDim, false, true);       // dQ += dS K
+        constexpr uint32_t idesc_t = idesc_bf16(kTileRows, kChunkKeys, true, true);       // dK^T, dV^T
+        int64_t gc = 0, qc = 0, u = 0;
+        Item it;
+        bool ok = true;
+        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+            if (it.nch == 0) continue;
+            if (!wait(kQFull, qc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int c = 0; c < it.nch; ++c, ++gc) {
+                if (!wait(kKFull, gc) || !wait(kVFull, gc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t off = kb * (kTileBytes / 4) + k * 32;
+                            const uint32_t koff = kb * (kKVBytes / 4) + k * 32;
+                            const uint32_t acc = (kb | k) ? 1u : 0u;
+                            mma_bf16(tmem + kTmemS, sdesc_sw128(sbase + kOffQ + off, 16, 1024),
+                                     sdesc_sw128(sbase + kOffK + koff, 16, 1024), idesc_n64, acc);
+                            mma_bf16(tmem + kTmemDP, sdesc_sw128(sbase + kOffDO + off, 16, 1024),
+                                     sdesc_sw128(sbase + kOffV + koff, 16, 1024), idesc_n64, acc);
+                        }
+                    }
+                    mma_commit(bars + kSDFull);
+                    mma_commit(bars + kVEmpty);
+                }
+                __syncwarp();
+                if (!wait(kPDSFull, gc) || (c == 0 && qc > 0 && !wait(kDQFree, qc - 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int k = 0; k < kChunkKeys / 16; ++k)
+                        mma_bf16(tmem + kTmemDQ, sdesc_sw128(sbase + kOffDS + k * 32, 16, 1024),
+                                 sdesc_sw128(sbase + kOffK + k * 2048, kKVBytes / 4, 1024), idesc_dq,
+                                 (c == 0 && k == 0) ? 0u : 1u);
+                    mma_commit(bars + kKEmpty);
+                    if (c == it.nch - 1) mma_commit(bars + kDQReady);
+                }
+                __syncwarp();
+                for (int h = 0; h < 2; ++h, ++u) {
+                    if (u > 0 && !wait(kFlushDone, u - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                            const uint32_t aoff = (2 * h) * (kTileBytes / 4) + kk * 2048;
+                            mma_bf16(tmem + kTmemDKT, sdesc_sw128(sbase + kOffQ + aoff, kTileBytes / 4, 1024),
+                                     sdesc_sw128(sbase + kOffDS + kk * 2048, kPBytes, 1024), idesc_t, kk ? 1u : 0u);
+                            mma_bf16(tmem + kTmemDVT, sdesc_sw128(sbase + kOffDO + aoff, kTileBytes / 4, 1024),
+                                     sdesc_sw128(sbase + kOffP + kk * 2048, kPBytes, 1024), idesc_t, kk ? 1u : 0u);
+                        }
+                        mma_commit(bars + kGradsFull);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) mma_commit(bars + kPDSEmpty);
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(bars + kQEmpty);
+            __syncwarp();
+            ++qc;
+        }
+        if (!ok && lane == 0) fail(3);
+        if (lane == 0) {
+            mma_commit(bars + kDrain);
+            if (!mbar_wait(bars + kDrain, 0, &zero, kWaitLimitNs)) fail(4);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------- softmax: P, dS; dQ epilogue ----------------
+        const int r = threadIdx.x;
+        const int qi = (int)(r / p.G), hl = (int)(r % p.G);
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        int64_t gc = 0, qc = 0;
+        Item it;
+        bool ok = true;
+        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+            const int64_t q = it.t * p.T + qi;
+            const int64_t h = it.g * p.G + hl;
+            const bool live = q < p.S_q;
+            __nv_bfloat16 *dqrow = p.dq + ((it.b * p.S_q + q) * p.Hq + h) * kHeadDim;
+            if (it.nch == 0) {
+                if (live) {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < kHeadDim / 8; ++i) reinterpret_cast<uint4 *>(dqrow)[i] = z;
+                }
+                continue;
+            }
+            const int64_t stat = (it.b * p.Hq + h) * p.S_q + q;
+            const float lse2 = live ? p.lse[stat] * kLog2e : 0.f;
+            const float delta = live ? p.delta[stat] : 0.f;
+            const uint64_t *mrow = p.tile_masks + it.tile * p.max_chunks * p.T + qi;
+            uint64_t mask_next = __ldg(mrow);
+            for (int c = 0; c < it.nch; ++c, ++gc) {
+                const uint64_t mask = mask_next;
+                if (c + 1 < it.nch) mask_next = __ldg(mrow + (c + 1) * p.T);
+                if (!wait(kSDFull, gc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sr[2][32], dr[2][32];
+                tmem_ld32(trow + kTmemS, sr[0]);
+                tmem_ld32(trow + kTmemS + 32, sr[1]);
+                tmem_ld32(trow + kTmemDP, dr[0]);
+                tmem_ld32(trow + kTmemDP + 32, dr[1]);
+                tmem_ld_wait();
+                if (gc > 0 && !wait(kPDSEmpty, gc - 1)) {
+                    ok = false;
+                    break;
+                }
+                uint32_t pk[32], dk[32];
+#pragma unroll
+                for (int j = 0; j < 64; j += 2) {
+                    float pv[2], dv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int jj = j + e;
+                        const bool in = (mask >> jj) & 1ull;
+                        const float s = __uint_as_float(sr[jj >> 5][jj & 31]);
+                        const float dp = __uint_as_float(dr[jj >> 5][jj & 31]);
+                        pv[e] = in ? ex2(s * p.sl2 - lse2) : 0.f;
+                        dv[e] = p.scale * pv[e] * (dp - delta);
+                    }
+                    pk[j >> 1] = pack_bf16(pv[0], pv[1]);
+                    dk[j >> 1] = pack_bf16(dv[0], dv[1]);
+                }
+                uint8_t *prow = smem + kOffP + r * 128;
+                uint8_t *drow = smem + kOffDS + r * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const int phys = (ch ^ (r & 7)) * 16;
+                    *reinterpret_cast<uint4 *>(prow + phys) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                                                                         pk[4 * ch + 3]);
+                    *reinterpret_cast<uint4 *>(drow + phys) = make_uint4(dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2],
+                                                                         dk[4 * ch + 3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bars + kPDSFull);
+            }
+            if (!ok) break;
+            if (!wait(kDQReady, qc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int blk = 0; blk < kHeadDim / 32; ++blk) {
+                uint32_t o[32];
+                tmem_ld32(trow + kTmemDQ + blk * 32, o);
+                tmem_ld_wait();
+                if (live) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[i + e]);
+                        reinterpret_cast<uint4 *>(dqrow + blk * 32 + i)[0] = f32x8_to_bf16(f);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bars + kDQFree);
+            ++qc;
+        }
+        if (!ok) fail(5);
+    } else {
+        // ---------------- flush: dK^T / dV^T -> fp32 scatter-add ----------------
+        const int quarter = warp & 3;
+        const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+        int64_t gc = 0, u = 0;
+        Item it;
+        bool ok = true;
+        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+            if (it.nch == 0) continue;
+            const int64_t row_stride = p.Hkv * kHeadDim;
+            float *dk_base = p.dk_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
+            float *dv_base = p.dv_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
+            for (int c = 0; c < it.nch; ++c, ++gc) {
+                const int32_t *keys = p.tile_keys + (it.tile * p.max_chunks + c) * kChunkKeys;
+                for (int h = 0; h < 2; ++h, ++u) {
+                    if (!wait(kGradsFull, u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t a[2][32], v[2][32];
+                    tmem_ld32(trow + kTmemDKT, a[0]);
+                    tmem_ld32(trow + kTmemDKT + 32, a[1]);
+                    tmem_ld32(trow + kTmemDVT, v[0]);
+                    tmem_ld32(trow + kTmemDVT + 32, v[1]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(bars + kFlushDone);
+                    int32_t prev = -1;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const int32_t key = __ldg(keys + j);
+                        if (key > prev) {  // keys ascend; the padding of a partial chunk repeats an earlier key
+                            const int64_t off = (int64_t)key * row_stride + h * 128;
+                            atomicAdd(dk_base + off, __uint_as_float(a[j >> 5][j & 31]));
+                            atomicAdd(dv_base + off, __uint_as_float(v[j >> 5][j & 31]));
+                            prev = key;
+                        }
+                    }
+                }
+                if (!ok) break;
+            }
+        }
+        if (!ok) fail(6);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool tc_backward_supported() { return tc_device_ok(); }
+
+bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t) {
+    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs;
+}
+
+cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_t s) {
+    const AttnArgs &a = bw.f;
+    BwdParams p;
+    memset(&p, 0, sizeof(p));
+    if (!tc_encode_tile_map(&p.q_map, a.q, a.Hq, a.S_q, a.B, a.qs2, a.qs1, a.qs0, a.G, t.T))
+        return cudaErrorInvalidValue;
+    if (!tc_encode_tile_map(&p.do_map, bw.dout, a.Hq, a.S_q, a.B, kHeadDim, a.Hq * kHeadDim,
+                            a.S_q * a.Hq * kHeadDim, a.G, t.T))
+        return cudaErrorInvalidValue;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int sms = tc_num_sms();
+    const int64_t g_per_launch = std::max<int64_t>(1, kMaxPairs / a.B);
+    p.B = a.B;
+    p.S_q = a.S_q;
+    p.S_kv = a.S_kv;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.G;
+    p.T = t.T;
+    p.n_tiles = t.n_tiles;
+    p.max_chunks = t.max_chunks;
+    p.sl2 = a.scale * kLog2e;
+    p.scale = a.scale;
+    p.tile_nchunks = t.tile_nchunks;
+    p.tile_keys = t.tile_keys;
+    p.tile_masks = t.tile_masks;
+    p.order = t.order;
+    p.lse = bw.lse;
+    p.delta = bw.delta;
+    p.dq = bw.dq;
+    p.dk_acc = bw.dk_acc;
+    p.dv_acc = bw.dv_acc;
+    p.status = a.status;
+    for (int64_t g0 = 0; g0 < a.Hkv; g0 += g_per_launch) {
+        const int64_t n_g = std::min<int64_t>(g_per_launch, a.Hkv - g0);
+        p.g0 = g0;
+        p.n_g = n_g;
+        p.n_items = n_g * a.B * t.n_tiles;
+        for (int64_t b = 0; b < a.B; ++b)
+            for (int64_t gi = 0; gi < n_g; ++gi) {
+                const int pair = (int)(b * n_g + gi);
+                const int64_t g = g0 + gi;
+                if (!tc_encode_rows_map(&p.kv_maps[2 * pair], a.k + b * a.ks0 + g * a.ks2, a.S_kv, a.ks1) ||
+                    !tc_encode_rows_map(&p.kv_maps[2 * pair + 1], a.v + b * a.vs0 + g * a.vs2, a.S_kv, a.vs1))
+                    return cudaErrorInvalidValue;
+            }
+        const int grid = (int)std::min<int64_t>(p.n_items, sms);
+        tc_bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace qsa

@@ -28,13 +28,9 @@
 // and the PV of chunk c-1.  Every mbarrier wait is bounded in time; on timeout
 // the kernel records QSA_ERR_TIMEOUT in the workspace status word, all roles
 // wind down, the TMEM is freed and the kernel returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <cmath>
 #include <algorithm>
+#include <cmath>
 #include <cstring>
-#include <mutex>
 
 #include "qsa_tc.cuh"
 #include "qsa_tc_ptx.cuh"
@@ -439,43 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     if (warp == 5) tmem_dealloc(tmem, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-bool encode_2d_rows(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems) {
-    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 2};
-    const cuuint32_t box[2] = {64, 1};
-    const cuuint32_t estr[2] = {1, 1};
-    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
-bool tc_forward_supported() {
-    static int ok = -1;
-    if (ok < 0) {
-        int dev = 0, major = 0, minor = 0;
-        ok = cudaGetDevice(&dev) == cudaSuccess &&
-             cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
-             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess && major == 10 &&
-             minor == 3 && encode_fn() != nullptr;
-    }
-    return ok == 1;
-}
+bool tc_forward_supported() { return tc_device_ok(); }
 
 bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t) {
     return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs;
@@ -484,25 +446,15 @@ bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t) {
 cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s) {
     FwdParams p;
     memset(&p, 0, sizeof(p));
-    {
-        const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)a.Hq, (cuuint64_t)a.S_q, (cuuint64_t)a.B};
-        const cuuint64_t strides[3] = {(cuuint64_t)a.qs2 * 2, (cuuint64_t)a.qs1 * 2, (cuuint64_t)a.qs0 * 2};
-        const cuuint32_t box[4] = {64, (cuuint32_t)a.G, (cuuint32_t)t.T, 1};
-        const cuuint32_t estr[4] = {1, 1, 1, 1};
-        if (encode_fn()(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<__nv_bfloat16 *>(a.q), dims, strides,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    if (!tc_encode_tile_map(&p.q_map, a.q, a.Hq, a.S_q, a.B, a.qs2, a.qs1, a.qs0, a.G, t.T))
+        return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = tc_num_sms();
     const int64_t g_per_launch = std::max<int64_t>(1, kMaxPairs / a.B);
     p.B = a.B;
     p.S_q = a.S_q;
@@ -528,8 +480,8 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
             for (int64_t gi = 0; gi < n_g; ++gi) {
                 const int pair = (int)(b * n_g + gi);
                 const int64_t g = g0 + gi;
-                if (!encode_2d_rows(&p.kv_maps[2 * pair], a.k + b * a.ks0 + g * a.ks2, a.S_kv, a.ks1) ||
-                    !encode_2d_rows(&p.kv_maps[2 * pair + 1], a.v + b * a.vs0 + g * a.vs2, a.S_kv, a.vs1))
+                if (!tc_encode_rows_map(&p.kv_maps[2 * pair], a.k + b * a.ks0 + g * a.ks2, a.S_kv, a.ks1) ||
+                    !tc_encode_rows_map(&p.kv_maps[2 * pair + 1], a.v + b * a.vs0 + g * a.vs2, a.S_kv, a.vs1))
                     return cudaErrorInvalidValue;
             }
         const int grid = (int)std::min<int64_t>(p.n_items, sms);

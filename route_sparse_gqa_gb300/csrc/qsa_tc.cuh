@@ -1,6 +1,8 @@
 // qsa_tc.cuh -- tile (tensor-core) path of libqsa: shared declarations.
 #pragma once
 
+#include <cuda.h>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -16,11 +18,23 @@ struct TileArgs {
     const int32_t *order;
 };
 
+// Host helpers shared by the tile kernels (qsa_tc_host.cu).
+bool tc_device_ok();  // current device is sm_103 and the TMA map encoder is reachable
+int tc_num_sms();
+// 2-D map over `rows` rows of 256 bf16 (row pitch in elements), box 64 x 1,
+// 128-byte swizzle: the operand of tile::gather4 row gathers.
+bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems);
+// 4-D map over a [B, S, H, 256] bf16 tensor (strides in elements), box
+// {64, G, T, 1}, 128-byte swizzle: one (T queries x G heads) tile per 64 columns.
+bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, int64_t B, int64_t sH, int64_t sS,
+                        int64_t sB, int64_t G, int64_t T);
+
 bool tc_forward_supported();
 bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t);
 cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s);
 
 bool tc_backward_supported();
+bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t);
 cudaError_t launch_tc_backward(const BwdArgs &b, const TileArgs &t, cudaStream_t s);
 
 }  // namespace qsa
