@@ -42,7 +42,7 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 320;  // warps 0-3 softmax, 4-7 flush, 8 producer, 9 MMA
-constexpr int kMaxPairs = 64;
+constexpr int kMaxPairs = kMaxKVPairs;
 constexpr uint32_t kTileBytes = kTileRows * kHeadDim * 2;    // 64 KiB (Q or dO tile)
 constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;     // 32 KiB
 constexpr uint32_t kPBytes = kTileRows * kChunkKeys * 2;     // 16 KiB
@@ -63,10 +63,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
     CUtensorMap q_map, do_map;          // 4-D {D, Hq, S_q, B}, box {64, G, T, 1}
-    CUtensorMap kv_maps[2 * kMaxPairs];  // per (b, g): K then V rows
+    KVMaps kv[kMaxPairs];               // per (b, g): K/V row-gather and 64-row-run maps
     int64_t B, S_q, S_kv, Hq, Hkv, G, T, n_tiles, max_chunks;
     int64_t g0, n_g, n_items;
     float sl2, scale;
+    uint64_t wait_limit_ns;  // bound of every pipeline wait
     const int32_t *tile_nchunks;
     const int32_t *tile_keys;
     const uint64_t *tile_masks;
@@ -133,14 +134,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         raise_status(p.status, QSA_ERR_TIMEOUT, kSiteTileBwdWait, info, blockIdx.x);
         *abort_flag = 1;
     };
-    auto wait = [&](int id, int64_t phase) { return mbar_wait(bars + id, (uint32_t)(phase & 1), abort_flag, kWaitLimitNs); };
+    auto wait = [&](int id, int64_t phase) {
+        return mbar_wait_warp(bars + id, (uint32_t)(phase & 1), abort_flag, p.wait_limit_ns);
+    };
 
     if (warp == 8) {
         // ---------------- producer ----------------
-        int64_t gc = 0, qc = 0;
+        int64_t gc = 0, qc = 0, v_issued = 0, k_issued = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
             if (qc > 0 && !wait(kQEmpty, qc - 1)) {
                 ok = false;
@@ -157,45 +160,55 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             }
             ++qc;
             const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
-            const CUtensorMap *kmap = &p.kv_maps[2 * pair], *vmap = &p.kv_maps[2 * pair + 1];
+            const KVMaps &maps = p.kv[pair];
             const int32_t *keys = p.tile_keys + it.tile * p.max_chunks * kChunkKeys;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 int4 kk = make_int4(0, 0, 0, 0);
                 if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
+                const int first = __shfl_sync(0xffffffffu, kk.x, 0), last = __shfl_sync(0xffffffffu, kk.w, 15);
+                const bool run = last - first == kChunkKeys - 1;  // ascending distinct keys: a contiguous run
                 if (gc > 0 && !wait(kVEmpty, gc - 1)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(bars + kVFull, kKVBytes);
                 __syncwarp();
-                if (lane < 16) {
-                    const uint32_t dst = sbase + kOffV + lane * 512;
+                if (run) {
+                    if (lane == 0)
+                        for (int kb = 0; kb < 4; ++kb)
+                            tma_load_2d(sbase + kOffV + kb * (kKVBytes / 4), &maps.v_run, bars + kVFull, kb * 64, first);
+                } else if (lane < 16) {
                     for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(dst + kb * (kKVBytes / 4), vmap, bars + kVFull, kb * 64, kk.x, kk.y, kk.z, kk.w);
+                        tma_gather4(sbase + kOffV + lane * 512 + kb * (kKVBytes / 4), &maps.v_rows, bars + kVFull,
+                                    kb * 64, kk.x, kk.y, kk.z, kk.w);
                 }
                 __syncwarp();
+                ++v_issued;
                 if (gc > 0 && !wait(kKEmpty, gc - 1)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) mbar_arrive_expect_tx(bars + kKFull, kKVBytes);
                 __syncwarp();
-                if (lane < 16) {
-                    const uint32_t dst = sbase + kOffK + lane * 512;
+                if (run) {
+                    if (lane == 0)
+                        for (int kb = 0; kb < 4; ++kb)
+                            tma_load_2d(sbase + kOffK + kb * (kKVBytes / 4), &maps.k_run, bars + kKFull, kb * 64, first);
+                } else if (lane < 16) {
                     for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(dst + kb * (kKVBytes / 4), kmap, bars + kKFull, kb * 64, kk.x, kk.y, kk.z, kk.w);
+                        tma_gather4(sbase + kOffK + lane * 512 + kb * (kKVBytes / 4), &maps.k_rows, bars + kKFull,
+                                    kb * 64, kk.x, kk.y, kk.z, kk.w);
                 }
                 __syncwarp();
+                ++k_issued;
             }
         }
         if (!ok && lane == 0) fail(1);
         // Drain every issued copy before the CTA can leave.
         if (lane == 0) {
             bool drained = true;
-            if (gc > 0) {
-                drained &= mbar_wait(bars + kVFull, (uint32_t)((gc - 1) & 1), &zero, kWaitLimitNs);
-                drained &= mbar_wait(bars + kKFull, (uint32_t)((gc - 1) & 1), &zero, kWaitLimitNs);
-            }
+            if (v_issued > 0) drained &= mbar_wait(bars + kVFull, (uint32_t)((v_issued - 1) & 1), &zero, kWaitLimitNs);
+            if (k_issued > 0) drained &= mbar_wait(bars + kKFull, (uint32_t)((k_issued - 1) & 1), &zero, kWaitLimitNs);
             if (qc > 0) drained &= mbar_wait(bars + kQFull, (uint32_t)((qc - 1) & 1), &zero, kWaitLimitNs);
             if (!drained) fail(2);
         }
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int64_t gc = 0, qc = 0, u = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
             if (!wait(kQFull, qc)) {
                 ok = false;
@@ -296,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int64_t gc = 0, qc = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             const int64_t q = it.t * p.T + qi;
             const int64_t h = it.g * p.G + hl;
             const bool live = q < p.S_q;
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int64_t gc = 0, u = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
             const int64_t row_stride = p.Hkv * kHeadDim;
             float *dk_base = p.dk_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
@@ -475,6 +488,7 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
     p.max_chunks = t.max_chunks;
     p.sl2 = a.scale * kLog2e;
     p.scale = a.scale;
+    p.wait_limit_ns = tc_wait_limit_ns(kWaitLimitNs);
     p.tile_nchunks = t.tile_nchunks;
     p.tile_keys = t.tile_keys;
     p.tile_masks = t.tile_masks;
@@ -491,13 +505,8 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
         p.n_g = n_g;
         p.n_items = n_g * a.B * t.n_tiles;
         for (int64_t b = 0; b < a.B; ++b)
-            for (int64_t gi = 0; gi < n_g; ++gi) {
-                const int pair = (int)(b * n_g + gi);
-                const int64_t g = g0 + gi;
-                if (!tc_encode_rows_map(&p.kv_maps[2 * pair], a.k + b * a.ks0 + g * a.ks2, a.S_kv, a.ks1) ||
-                    !tc_encode_rows_map(&p.kv_maps[2 * pair + 1], a.v + b * a.vs0 + g * a.vs2, a.S_kv, a.vs1))
-                    return cudaErrorInvalidValue;
-            }
+            for (int64_t gi = 0; gi < n_g; ++gi)
+                if (!tc_encode_kv_maps(&p.kv[b * n_g + gi], a, b, g0 + gi)) return cudaErrorInvalidValue;
         const int grid = (int)std::min<int64_t>(p.n_items, sms);
         tc_bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
         cudaError_t e = cudaGetLastError();

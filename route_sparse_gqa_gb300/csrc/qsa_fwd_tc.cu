@@ -42,7 +42,7 @@ using namespace ptx;
 
 constexpr int kStages = 2;
 constexpr int kThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
-constexpr int kMaxPairs = 64;  // (b, g) tensor-map pairs per launch
+constexpr int kMaxPairs = kMaxKVPairs;  // (b, g) tensor-map sets per launch
 constexpr uint32_t kQBytes = kTileRows * kHeadDim * 2;       // 64 KiB
 constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;     // 32 KiB per K or V chunk
 constexpr uint32_t kPBytes = kTileRows * kChunkKeys * 2;     // 16 KiB
@@ -64,11 +64,12 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 struct FwdParams {
     CUtensorMap q_map;                  // 4-D {D, Hq, S_q, B}, box {64, G, T, 1}
-    CUtensorMap kv_maps[2 * kMaxPairs];  // per (b, g): K then V, 2-D {D, S_kv}, box {64, 1}
+    KVMaps kv[kMaxPairs];               // per (b, g): K/V row-gather and 64-row-run maps
     int64_t B, S_q, Hq, G, T, n_tiles, max_chunks;
     int64_t g0, n_g;   // KV heads handled by this launch
     int64_t n_items;   // n_g * B * n_tiles
     float sl2;         // softmax_scale * log2(e)
+    uint64_t wait_limit_ns;  // bound of every pipeline wait
     const int32_t *tile_nchunks;
     const int32_t *tile_keys;
     const uint64_t *tile_masks;
@@ -168,9 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         int64_t last_gc[kStages];
         for (int i = 0; i < kStages; ++i) last_gc[i] = -1;
         Item it;
-        for (int64_t round = 0; item_at(p, round, it) && !*abort_flag; ++round) {
+        for (int64_t round = 0; item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
-            if (qc > 0 && !mbar_wait(bar.q_empty, (qc - 1) & 1, abort_flag, kWaitLimitNs)) {
+            if (qc > 0 && !mbar_wait_warp(bar.q_empty, (qc - 1) & 1, abort_flag, p.wait_limit_ns)) {
                 if (lane == 0) fail(kSiteTileFwdWait, 1);
                 break;
             }
@@ -182,36 +183,43 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             }
             ++qc;  // Q loads issued so far
             const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
-            const CUtensorMap *kmap = &p.kv_maps[2 * pair], *vmap = &p.kv_maps[2 * pair + 1];
+            const KVMaps &maps = p.kv[pair];
             const int32_t *keys = p.tile_keys + it.tile * p.max_chunks * kChunkKeys;
             const uint64_t *masks = p.tile_masks + it.tile * p.max_chunks * p.T;
             bool ok = true;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 const int s = (int)(gc % kStages);
-                if (gc >= kStages && !mbar_wait(bar.kv_empty + s, ((gc / kStages) - 1) & 1, abort_flag, kWaitLimitNs)) {
+                // The chunk's keys are independent of the stage: fetch them before waiting for it.
+                int4 kk = make_int4(0, 0, 0, 0);
+                if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
+                const int first = __shfl_sync(0xffffffffu, kk.x, 0), last = __shfl_sync(0xffffffffu, kk.w, 15);
+                const bool run = last - first == kChunkKeys - 1;  // ascending distinct keys: a contiguous run
+                if (gc >= kStages && !mbar_wait_warp(bar.kv_empty + s, ((gc / kStages) - 1) & 1, abort_flag, p.wait_limit_ns)) {
                     if (lane == 0) fail(kSiteTileFwdWait, 2);
                     ok = false;
                     break;
                 }
-                int4 kk = make_int4(0, 0, 0, 0);
-                if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
+                const uint32_t kdst = sbase + kOffK + s * kKVBytes, vdst = sbase + kOffV + s * kKVBytes;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(bar.k_full + s, kKVBytes + (uint32_t)(p.T * 8));
                     bulk_load(sbase + kOffMask + s * 256, masks + c * p.T, (uint32_t)(p.T * 8), bar.k_full + s);
+                    mbar_arrive_expect_tx(bar.v_full + s, kKVBytes);
                 }
                 __syncwarp();
-                if (lane < 16) {
-                    const uint32_t dst = sbase + kOffK + s * kKVBytes + lane * 512;
+                if (run) {
+                    if (lane == 0) {
+                        for (int kb = 0; kb < 4; ++kb)
+                            tma_load_2d(kdst + kb * (kKVBytes / 4), &maps.k_run, bar.k_full + s, kb * 64, first);
+                        for (int kb = 0; kb < 4; ++kb)
+                            tma_load_2d(vdst + kb * (kKVBytes / 4), &maps.v_run, bar.v_full + s, kb * 64, first);
+                    }
+                } else if (lane < 16) {
                     for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(dst + kb * (kKVBytes / 4), kmap, bar.k_full + s, kb * 64, kk.x, kk.y, kk.z, kk.w);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(bar.v_full + s, kKVBytes);
-                __syncwarp();
-                if (lane < 16) {
-                    const uint32_t dst = sbase + kOffV + s * kKVBytes + lane * 512;
+                        tma_gather4(kdst + lane * 512 + kb * (kKVBytes / 4), &maps.k_rows, bar.k_full + s, kb * 64,
+                                    kk.x, kk.y, kk.z, kk.w);
                     for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(dst + kb * (kKVBytes / 4), vmap, bar.v_full + s, kb * 64, kk.x, kk.y, kk.z, kk.w);
+                        tma_gather4(vdst + lane * 512 + kb * (kKVBytes / 4), &maps.v_rows, bar.v_full + s, kb * 64,
+                                    kk.x, kk.y, kk.z, kk.w);
                 }
                 __syncwarp();
                 last_gc[s] = gc;
@@ -241,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         bool ok = true;
         auto issue_pv = [&](int64_t g2, bool first) -> bool {
             const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
-            if (!mbar_wait(bar.p_full + sb, (g2 >> 1) & 1, abort_flag, kWaitLimitNs)) return false;
-            if (!mbar_wait(bar.v_full + s, (g2 / kStages) & 1, abort_flag, kWaitLimitNs)) return false;
-            if (first && qc > 0 && !mbar_wait(bar.o_free, (qc - 1) & 1, abort_flag, kWaitLimitNs)) return false;
+            if (!mbar_wait_warp(bar.p_full + sb, (g2 >> 1) & 1, abort_flag, p.wait_limit_ns)) return false;
+            if (!mbar_wait_warp(bar.v_full + s, (g2 / kStages) & 1, abort_flag, p.wait_limit_ns)) return false;
+            if (first && qc > 0 && !mbar_wait_warp(bar.o_free, (qc - 1) & 1, abort_flag, p.wait_limit_ns)) return false;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t pa = sbase + kOffP + sb * kPBytes;
@@ -260,16 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             __syncwarp();
             return true;
         };
-        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
-            if (!mbar_wait(bar.q_full, qc & 1, abort_flag, kWaitLimitNs)) {
+            if (!mbar_wait_warp(bar.q_full, qc & 1, abort_flag, p.wait_limit_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 const int s = (int)(gc % kStages), sb = (int)(gc & 1);
-                if (!mbar_wait(bar.k_full + s, (gc / kStages) & 1, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait_warp(bar.k_full + s, (gc / kStages) & 1, abort_flag, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         int64_t gc = 0, qc = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it) && !*abort_flag; ++round) {
+        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             const int64_t q = it.t * p.T + qi;
             const int64_t h = it.g * p.G + hl;
             const bool live = q < p.S_q;
@@ -334,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             float m = -INFINITY, l = 0.f;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 const int s = (int)(gc % kStages), sb = (int)(gc & 1);
-                if (!mbar_wait(bar.s_full + sb, (gc >> 1) & 1, abort_flag, kWaitLimitNs) ||
-                    !mbar_wait(bar.k_full + s, (gc / kStages) & 1, abort_flag, kWaitLimitNs)) {
+                if (!mbar_wait_warp(bar.s_full + sb, (gc >> 1) & 1, abort_flag, p.wait_limit_ns) ||
+                    !mbar_wait_warp(bar.k_full + s, (gc / kStages) & 1, abort_flag, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -354,12 +362,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 const bool need = (m != -INFINITY) && (mx > m + kRescaleThreshold);
                 if (m == -INFINITY) m = mx;  // first keys of this row: nothing accumulated yet
+                // o_ready completes once per PV.  These warps consume every phase exactly once and in
+                // order (the PV of chunk c-1 during chunk c, the item's last PV in the epilogue), so a
+                // parity wait always targets the oldest open phase and is never ambiguous.
+                bool prev_pv_seen = (c == 0);
                 if (__any_sync(0xffffffffu, need)) {
-                    // Rescale O: wait until the previous chunk's PV has landed in TMEM.
-                    if (!mbar_wait(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, kWaitLimitNs)) {
+                    // Rescale O: the previous chunk's PV must have landed in TMEM first.
+                    if (!mbar_wait_warp(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
+                    prev_pv_seen = true;
                     tc_fence_after();
                     const float alpha = need ? ex2(m - mx) : 1.f;
 #pragma unroll 1
@@ -394,13 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     *reinterpret_cast<uint4 *>(prow + phys * 16) =
                         make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
                 }
+                if (!prev_pv_seen && !mbar_wait_warp(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, p.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar.p_full + sb);
             }
             if (!ok) break;
-            // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)).
-            if (!mbar_wait(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, kWaitLimitNs)) {
+            // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)) once the item's last PV has landed.
+            if (!mbar_wait_warp(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, p.wait_limit_ns)) {
                 ok = false;
                 break;
             }
@@ -464,6 +481,7 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
     p.n_tiles = t.n_tiles;
     p.max_chunks = t.max_chunks;
     p.sl2 = a.scale * kLog2e;
+    p.wait_limit_ns = tc_wait_limit_ns(kWaitLimitNs);
     p.tile_nchunks = t.tile_nchunks;
     p.tile_keys = t.tile_keys;
     p.tile_masks = t.tile_masks;
@@ -477,13 +495,8 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
         p.n_g = n_g;
         p.n_items = n_g * a.B * t.n_tiles;
         for (int64_t b = 0; b < a.B; ++b)
-            for (int64_t gi = 0; gi < n_g; ++gi) {
-                const int pair = (int)(b * n_g + gi);
-                const int64_t g = g0 + gi;
-                if (!tc_encode_rows_map(&p.kv_maps[2 * pair], a.k + b * a.ks0 + g * a.ks2, a.S_kv, a.ks1) ||
-                    !tc_encode_rows_map(&p.kv_maps[2 * pair + 1], a.v + b * a.vs0 + g * a.vs2, a.S_kv, a.vs1))
-                    return cudaErrorInvalidValue;
-            }
+            for (int64_t gi = 0; gi < n_g; ++gi)
+                if (!tc_encode_kv_maps(&p.kv[b * n_g + gi], a, b, g0 + gi)) return cudaErrorInvalidValue;
         const int grid = (int)std::min<int64_t>(p.n_items, sms);
         tc_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
         cudaError_t e = cudaGetLastError();

@@ -7,7 +7,10 @@
 //   route_rows_kernel  one CTA per query row: read the row's K route slots in
 //                      their own width (int32 or int64), keep 0 <= id < S_kv
 //                      (invalid values, huge int64 included, never reach an
-//                      index), bitonic-sort in shared memory, drop repeats.
+//                      index), set their bits in a shared-memory bitmap over
+//                      the row's id range and read the bitmap back in order
+//                      (sorted, repeats gone); a bitonic sort handles rows
+//                      whose ids are spread over a very wide range.
 //                      Output: ascending unique IDs (int32, -1 tail) + count.
 //   route_tiles_kernel one CTA per tile of T consecutive query rows: the union
 //                      of the rows' ID sets, ascending, cut into chunks of 64
@@ -18,6 +21,8 @@
 //                      only T x W bits of it, never in HBM).
 //   route_order_kernel counting sort of tiles by chunk count, heaviest first,
 //                      for the attention kernels' static schedule.
+#include <algorithm>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -26,6 +31,8 @@ namespace {
 constexpr int kRowThreads = 256;
 constexpr int kTileThreads = 256;
 constexpr int kTileWindow = 4096;  // keys per window of the shared-memory membership table
+constexpr int kRowWindowBits = 65536;  // keys per window of a row's shared-memory bitmap (8 KiB)
+constexpr int kRowMaxWindows = 8;      // wider rows fall back to the bitonic sort
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -55,48 +62,113 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int &t
     return r;
 }
 
+__device__ __forceinline__ int64_t load_route(const RowsArgs &a, int64_t b, int64_t q, int64_t i) {
+    const int64_t off = b * a.rs0 + q * a.rs1 + i * a.rs2;
+    return a.route_bits == 64 ? static_cast<const int64_t *>(a.routes)[off]
+                              : (int64_t) static_cast<const int32_t *>(a.routes)[off];
+}
+
+// Sorting by bitmap: the row's valid ids set bits in a shared-memory bitmap
+// over a window of key space; a popcount scan over the bitmap then yields the
+// ids ascending with repeats gone.  Cost O(K + range/32) per window; rows whose
+// ids span more than kRowMaxWindows windows use the bitonic sort instead.
 __global__ void __launch_bounds__(kRowThreads) route_rows_kernel(RowsArgs a, int P) {
-    extern __shared__ int32_t srt[];  // [P]
+    extern __shared__ uint32_t rsm[];  // bitmap [kRowWindowBits/32] or bitonic buffer [P]
     __shared__ int warp_tot[33];
+    __shared__ int64_t red_lo[kRowThreads / 32], red_hi[kRowThreads / 32];
     const int64_t row = blockIdx.x;
     const int64_t b = row / a.S_q, q = row % a.S_q;
-    const int tid = threadIdx.x;
-    // Validate in the route's own width before narrowing (fa4_qsa _preprocess).
-    for (int i = tid; i < P; i += blockDim.x) {
-        int32_t v = INT32_MAX;
-        if (i < a.K) {
-            const int64_t off = b * a.rs0 + q * a.rs1 + (int64_t)i * a.rs2;
-            const int64_t x = a.route_bits == 64 ? static_cast<const int64_t *>(a.routes)[off]
-                                                 : (int64_t) static_cast<const int32_t *>(a.routes)[off];
-            if (x >= 0 && x < a.S_kv) v = (int32_t)x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    int32_t *out = a.ids + row * a.K;
+
+    // Range of the valid ids (validity tested in the route's own width).
+    int64_t lo = INT64_MAX, hi = -1;
+    for (int64_t i = tid; i < a.K; i += blockDim.x) {
+        const int64_t x = load_route(a, b, q, i);
+        if (x >= 0 && x < a.S_kv) {
+            lo = min(lo, x);
+            hi = max(hi, x);
         }
-        srt[i] = v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        red_lo[warp] = lo;
+        red_hi[warp] = hi;
     }
     __syncthreads();
-    for (int k = 2; k <= P; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < P; i += blockDim.x) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const int32_t x = srt[i], y = srt[ixj];
-                    if ((x > y) == ((i & k) == 0)) {
-                        srt[i] = y;
-                        srt[ixj] = x;
-                    }
-                }
+    lo = red_lo[0];
+    hi = red_hi[0];
+    for (int w = 1; w < nwarps; ++w) {
+        lo = min(lo, red_lo[w]);
+        hi = max(hi, red_hi[w]);
+    }
+    int total = 0;
+    if (hi >= 0 && (hi - lo) / kRowWindowBits < kRowMaxWindows) {
+        for (int64_t w0 = lo; w0 <= hi; w0 += kRowWindowBits) {
+            const int64_t span = (hi - w0 + 1) < kRowWindowBits ? (hi - w0 + 1) : (int64_t)kRowWindowBits;
+            const int nwords = (int)((span + 31) / 32);
+            for (int i = tid; i < nwords; i += blockDim.x) rsm[i] = 0u;
+            __syncthreads();
+            for (int64_t i = tid; i < a.K; i += blockDim.x) {
+                const int64_t x = load_route(a, b, q, i);
+                if (x >= w0 && x < w0 + span) atomicOr(&rsm[(x - w0) >> 5], 1u << ((x - w0) & 31));
             }
             __syncthreads();
+            const int per = (nwords + blockDim.x - 1) / blockDim.x;
+            const int s0 = min(nwords, tid * per), s1 = min(nwords, s0 + per);
+            int local = 0;
+            for (int i = s0; i < s1; ++i) local += __popc(rsm[i]);
+            int win_total;
+            int pos = total + block_exclusive_scan(local, warp_tot, win_total);
+            for (int i = s0; i < s1; ++i) {
+                uint32_t bits = rsm[i];
+                while (bits) {
+                    const int bit = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    out[pos++] = (int32_t)(w0 + i * 32 + bit);
+                }
+            }
+            total += win_total;
+            __syncthreads();
         }
+    } else if (hi >= 0) {
+        int32_t *srt = reinterpret_cast<int32_t *>(rsm);
+        for (int i = tid; i < P; i += blockDim.x) {
+            int32_t v = INT32_MAX;
+            if (i < a.K) {
+                const int64_t x = load_route(a, b, q, i);
+                if (x >= 0 && x < a.S_kv) v = (int32_t)x;
+            }
+            srt[i] = v;
+        }
+        __syncthreads();
+        for (int k = 2; k <= P; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                for (int i = tid; i < P; i += blockDim.x) {
+                    const int ixj = i ^ j;
+                    if (ixj > i) {
+                        const int32_t x = srt[i], y = srt[ixj];
+                        if ((x > y) == ((i & k) == 0)) {
+                            srt[i] = y;
+                            srt[ixj] = x;
+                        }
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        const int seg = (P + blockDim.x - 1) / blockDim.x;
+        const int s0 = min(P, tid * seg), s1 = min(P, s0 + seg);
+        int local = 0;
+        for (int i = s0; i < s1; ++i) local += srt[i] != INT32_MAX && (i == 0 || srt[i] != srt[i - 1]);
+        int pos = block_exclusive_scan(local, warp_tot, total);
+        for (int i = s0; i < s1; ++i)
+            if (srt[i] != INT32_MAX && (i == 0 || srt[i] != srt[i - 1])) out[pos++] = srt[i];
     }
-    const int seg = (P + blockDim.x - 1) / blockDim.x;
-    const int s0 = min(P, tid * seg), s1 = min(P, s0 + seg);
-    int local = 0;
-    for (int i = s0; i < s1; ++i) local += srt[i] != INT32_MAX && (i == 0 || srt[i] != srt[i - 1]);
-    int total;
-    int pos = block_exclusive_scan(local, warp_tot, total);
-    int32_t *out = a.ids + row * a.K;
-    for (int i = s0; i < s1; ++i)
-        if (srt[i] != INT32_MAX && (i == 0 || srt[i] != srt[i - 1])) out[pos++] = srt[i];
     for (int64_t i = total + tid; i < a.K; i += blockDim.x) out[i] = -1;
     if (tid == 0) a.counts[row] = total;
 }
@@ -250,7 +322,7 @@ __global__ void __launch_bounds__(kOrderThreads) route_order_kernel(const int32_
 cudaError_t launch_route_rows(const RowsArgs &a, cudaStream_t s) {
     int P = 32;
     while (P < a.K) P <<= 1;
-    const size_t smem = (size_t)P * sizeof(int32_t);
+    const size_t smem = std::max<size_t>((size_t)P * sizeof(int32_t), kRowWindowBits / 8);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(route_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

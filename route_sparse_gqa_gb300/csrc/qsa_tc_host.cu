@@ -3,6 +3,7 @@
 // device capability checks.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "qsa_tc.cuh"
@@ -41,6 +42,14 @@ int tc_num_sms() {
     return sms > 0 ? sms : 1;
 }
 
+uint64_t tc_wait_limit_ns(uint64_t fallback) {
+    const char *env = std::getenv("QSA_DEBUG_WAIT_LIMIT_NS");
+    if (!env || !*env) return fallback;
+    char *end = nullptr;
+    const unsigned long long v = std::strtoull(env, &end, 10);
+    return (end && *end == '\0') ? (uint64_t)v : fallback;
+}
+
 bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems) {
     const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 2};
@@ -49,6 +58,22 @@ bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t 
     return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_encode_run_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems) {
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kChunkKeys};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_encode_kv_maps(KVMaps *m, const AttnArgs &a, int64_t b, int64_t g) {
+    const __nv_bfloat16 *kb = a.k + b * a.ks0 + g * a.ks2, *vb = a.v + b * a.vs0 + g * a.vs2;
+    return tc_encode_rows_map(&m->k_rows, kb, a.S_kv, a.ks1) && tc_encode_rows_map(&m->v_rows, vb, a.S_kv, a.vs1) &&
+           tc_encode_run_map(&m->k_run, kb, a.S_kv, a.ks1) && tc_encode_run_map(&m->v_run, vb, a.S_kv, a.vs1);
 }
 
 bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, int64_t B, int64_t sH, int64_t sS,

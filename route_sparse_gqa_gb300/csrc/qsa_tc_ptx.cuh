@@ -42,11 +42,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds (or at once when *abort is set by another role) and
-// returns false; the caller then records a timeout and winds down.
+// returns false; the caller then records a timeout and winds down.  A limit of
+// 0 (test hook) only tests the phase once, without blocking.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort,
                                           uint64_t limit_ns) {
+    if (limit_ns == 0) return mbar_test_wait(bar, parity);
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
@@ -56,6 +70,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
             if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
+}
+
+// The same wait executed by a whole warp, with one verdict for the warp: if any
+// lane gave up, every lane reports failure, so the warp never splits around
+// the warp-collective instructions that follow a wait.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const volatile int *abort,
+                                               uint64_t limit_ns) {
+    const bool ok = mbar_wait(bar, parity, abort, limit_ns);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // ---- TMA ----
@@ -69,6 +92,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
         "[%6];" ::"r"(dst),
         "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint64_t *bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(m), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -91,3 +91,23 @@ def test_workload_full_size(index):
             expect = do_b[live][:, g * G:(g + 1) * G].sum((0, 1))
             scale_v = np.abs(do_b[live][:, g * G:(g + 1) * G]).sum((0, 1)) + 1.0
             assert np.all(np.abs(dv_sum - expect) <= 1e-3 * scale_v), f"sum dV b{b} g{g}"
+
+
+def test_right_padded_workload_every_element():
+    """Every output element of the right-padded workload against the full oracle
+    (forward and backward, ~15 s of oracle time).  Short tiles there (two chunks)
+    end their items right after their first PV, which exposes any barrier-phase
+    mistake between the PV and the epilogue that sampled rows can miss."""
+    case = W.make_case(1)
+    w = case.workload
+    out = run_library(case.q, case.k, case.v, case.do, case.routes, w.softmax_scale, fp32_dkdv=True)
+    qd, kd, vd, dod = f64(case.q), f64(case.k), f64(case.v), f64(case.do)
+    o_ref, lse_ref = oracle.forward(qd, kd, vd, case.routes, w.softmax_scale)
+    dq_ref, dk_ref, dv_ref = oracle.backward(qd, kd, vd, case.routes, dod, w.softmax_scale)
+    assert_close("O", out["o"], o_ref)
+    assert_lse_close(out["lse"], lse_ref)
+    assert_close("dQ", out["dq"], dq_ref)
+    assert_close("dK", out["dk"], dk_ref)
+    assert_close("dV", out["dv"], dv_ref)
+    assert_close("dK fp32", out["dk32"], dk_ref)
+    assert_close("dV fp32", out["dv32"], dv_ref)

@@ -166,3 +166,26 @@ def test_autograd_matches_explicit_backward():
     assert torch.equal(o.detach(), o2)
     for a, b in ((qt.grad, dq), (kt.grad, dk), (vt.grad, dv)):
         assert torch.allclose(a.float(), b.float(), rtol=1e-2, atol=1e-2)
+
+
+def test_route_sets_wide_and_narrow_ranges():
+    """Rows whose ids span a huge key range (sorted by the bitonic fallback) next
+    to narrow rows (sorted through the shared-memory bitmap): bit-exact."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    rng = np.random.default_rng(31)
+    S_q, S_kv, K = 24, 1_500_000, 96
+    routes = rng.integers(-4, S_kv + 4, size=(1, S_q, K)).astype(np.int64)
+    routes[0, ::3] = rng.integers(1000, 1200, size=(S_q // 3 + (S_q % 3 > 0), K))  # narrow rows
+    routes[0, 1::5, :10] = 2**45 + 3
+    routes[0, 7] = -1
+    dev = torch.device("cuda:0")
+    q = torch.zeros(1, S_q, 16, 256, dtype=torch.bfloat16, device=dev)
+    k = torch.zeros(1, S_kv, 2, 256, dtype=torch.bfloat16, device=dev)
+    plan = qsa.preprocess(q, k, k, torch.from_numpy(routes).to(dev))
+    ids, counts = plan.route_sets()
+    ids_ref, counts_ref = oracle.route_sets(routes, S_kv)
+    assert np.array_equal(counts.cpu().numpy(), counts_ref)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
