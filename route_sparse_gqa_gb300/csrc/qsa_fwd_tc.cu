@@ -6,28 +6,34 @@
 // the tile the ascending union of its rows' route sets cut into chunks of 64
 // keys, with a 64-bit membership mask per (chunk, query).  For every chunk:
 //
-//   producer warp   gathers the chunk's 64 K rows and 64 V rows of head g from
-//                   HBM/L2 with TMA tile::gather4 (four arbitrary rows per
-//                   instruction) into 128-byte-swizzled shared memory, plus
-//                   the chunk's masks (bulk copy);
+//   producer warp   loads the chunk's 64 K rows and 64 V rows of head g into
+//                   128-byte-swizzled shared memory: four 64-row TMA tile boxes
+//                   when the keys form one contiguous run, otherwise TMA
+//                   tile::gather4 (four arbitrary rows per instruction);
 //   MMA warp        S = Q K^T (M=128, N=64, K=256) into TMEM, later
 //                   O += P V (M=128, N=256, K=64) into a TMEM accumulator;
 //   softmax warps   (4 warps, thread i owns TMEM lane / row i) read S, apply
-//                   the row's membership bits, run the online softmax in fp32
-//                   (base-2, scale folded in, lazy rescale of O when the
-//                   running max grows by more than 2^8), write P as BF16 into
-//                   shared memory for the PV MMA, and finally normalise O,
-//                   store it as BF16 and write LSE (natural log).
+//                   the row's membership bits (read from global memory one
+//                   chunk ahead), run the online softmax in fp32 (base-2,
+//                   scale folded in, lazy rescale of O when the running max
+//                   grows by more than 2^8), write P as BF16 into shared memory
+//                   for the PV MMA, and finally normalise O, store it as BF16
+//                   and write LSE (natural log).
 //
 // Every K/V row gathered once into shared memory serves all G heads of the
 // group and all T queries of the tile that route to it.  Keys a query does not
 // route to get P = 0 exactly, so the result is the exact route-set softmax.
 //
-// Pipelining: two K/V stages, two S buffers in TMEM and two P buffers, so the
-// gather of chunk c+1 and the QK^T of chunk c+1 overlap the softmax of chunk c
-// and the PV of chunk c-1.  Every mbarrier wait is bounded in time; on timeout
-// the kernel records QSA_ERR_TIMEOUT in the workspace status word, all roles
-// wind down, the TMEM is freed and the kernel returns.
+// Pipelining: K and V have separate two-stage rings.  A K stage is released as
+// soon as its S MMA completes and a V stage when its PV MMA completes; the
+// producer loads K of chunk c alongside V of chunk c-1, and the MMA warp keeps
+// S two chunks ahead of PV (order S0 S1 PV0 S2 PV1 S3 ...), so neither the
+// gather latency nor the PV waits sit on the softmax's critical path.  Two S
+// buffers in TMEM and two P buffers in shared memory alternate by chunk.  Every
+// mbarrier phase is consumed in order by each waiter, every wait is bounded in
+// time; on timeout the kernel records QSA_ERR_TIMEOUT in the workspace status
+// word, all roles wind down, in-flight copies and MMAs drain, the TMEM is freed
+// and the kernel returns.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -50,9 +56,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
 constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
-constexpr uint32_t kOffMask = kOffP + 2 * kPBytes;            // kStages x 256 B
-constexpr uint32_t kOffBar = kOffMask + kStages * 256;
-constexpr uint32_t kNumBars = 5 + 3 * kStages + 2 * 2;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kNumBars = 5 + 4 * kStages + 2 * 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
@@ -99,8 +104,8 @@ __device__ __forceinline__ bool item_at(const FwdParams &p, int64_t round, Item 
 
 struct Bars {
     uint64_t *q_full, *q_empty, *o_ready, *o_free, *drain;
-    uint64_t *k_full, *v_full, *kv_empty;  // [kStages]
-    uint64_t *s_full, *p_full;             // [2]
+    uint64_t *k_full, *k_empty, *v_full, *v_empty;  // [kStages] each
+    uint64_t *s_full, *p_full;                      // [2]
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
@@ -112,11 +117,25 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     r.o_free = b + 3;
     r.drain = b + 4;
     r.k_full = b + 5;
-    r.v_full = b + 5 + kStages;
-    r.kv_empty = b + 5 + 2 * kStages;
-    r.s_full = b + 5 + 3 * kStages;
-    r.p_full = b + 5 + 3 * kStages + 2;
+    r.k_empty = b + 5 + kStages;
+    r.v_full = b + 5 + 2 * kStages;
+    r.v_empty = b + 5 + 3 * kStages;
+    r.s_full = b + 5 + 4 * kStages;
+    r.p_full = b + 5 + 4 * kStages + 2;
     return r;
+}
+
+// Loads the 64 K or V rows of one chunk into a stage: four 64-row tile boxes
+// when the keys form one contiguous run, else 16 lanes x 4 tile::gather4.
+__device__ __forceinline__ void load_chunk_rows(uint32_t dst, const CUtensorMap *run_map, const CUtensorMap *rows_map,
+                                                uint64_t *bar, bool run, int first, const int4 &kk, int lane) {
+    if (run) {
+        if (lane == 0)
+            for (int kb = 0; kb < 4; ++kb) tma_load_2d(dst + kb * (kKVBytes / 4), run_map, bar, kb * 64, first);
+    } else if (lane < 16) {
+        for (int kb = 0; kb < 4; ++kb)
+            tma_gather4(dst + lane * 512 + kb * (kKVBytes / 4), rows_map, bar, kb * 64, kk.x, kk.y, kk.z, kk.w);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
@@ -136,8 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         mbar_init(bar.drain, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar.k_full + s, 1);
+            mbar_init(bar.k_empty + s, 1);
             mbar_init(bar.v_full + s, 1);
-            mbar_init(bar.kv_empty + s, 1);
+            mbar_init(bar.v_empty + s, 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar.s_full + s, 1);
@@ -157,22 +177,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int zero = 0;
 
     auto fail = [&](unsigned where, unsigned info) {
         raise_status(p.status, QSA_ERR_TIMEOUT, where, info, blockIdx.x);
         *abort_flag = 1;
     };
+    auto wait = [&](uint64_t *b, int64_t phase) {
+        return mbar_wait_warp(b, (uint32_t)(phase & 1), abort_flag, p.wait_limit_ns);
+    };
 
     if (warp == 4) {
         // ---------------- producer ----------------
+        // K rows of chunk c are loaded one step ahead of the V rows of chunk c-1: S needs K
+        // early, PV needs V only after the softmax.  K and V have separate two-stage rings,
+        // released by S and by PV respectively.
         int64_t gc = 0, qc = 0;
-        int64_t last_gc[kStages];
-        for (int i = 0; i < kStages; ++i) last_gc[i] = -1;
+        int64_t last_k[kStages] = {-1, -1}, last_v[kStages] = {-1, -1};
         Item it;
-        for (int64_t round = 0; item_at(p, round, it); ++round) {
+        bool ok = true;
+        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
-            if (qc > 0 && !mbar_wait_warp(bar.q_empty, (qc - 1) & 1, abort_flag, p.wait_limit_ns)) {
-                if (lane == 0) fail(kSiteTileFwdWait, 1);
+            if (qc > 0 && !wait(bar.q_empty, qc - 1)) {
+                ok = false;
                 break;
             }
             if (lane == 0) {
@@ -181,77 +208,104 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     tma_load_4d(sbase + kOffQ + kb * (kQBytes / 4), &p.q_map, bar.q_full, kb * 64, (int)(it.g * p.G),
                                 (int)(it.t * p.T), (int)it.b);
             }
-            ++qc;  // Q loads issued so far
+            ++qc;
             const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
             const KVMaps &maps = p.kv[pair];
             const int32_t *keys = p.tile_keys + it.tile * p.max_chunks * kChunkKeys;
-            const uint64_t *masks = p.tile_masks + it.tile * p.max_chunks * p.T;
-            bool ok = true;
-            for (int c = 0; c < it.nch; ++c, ++gc) {
-                const int s = (int)(gc % kStages);
-                // The chunk's keys are independent of the stage: fetch them before waiting for it.
+            int4 kk_prev = make_int4(0, 0, 0, 0);
+            int first_prev = 0;
+            bool run_prev = false;
+            for (int c = 0; c <= it.nch; ++c) {
                 int4 kk = make_int4(0, 0, 0, 0);
-                if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
-                const int first = __shfl_sync(0xffffffffu, kk.x, 0), last = __shfl_sync(0xffffffffu, kk.w, 15);
-                const bool run = last - first == kChunkKeys - 1;  // ascending distinct keys: a contiguous run
-                if (gc >= kStages && !mbar_wait_warp(bar.kv_empty + s, ((gc / kStages) - 1) & 1, abort_flag, p.wait_limit_ns)) {
-                    if (lane == 0) fail(kSiteTileFwdWait, 2);
-                    ok = false;
-                    break;
-                }
-                const uint32_t kdst = sbase + kOffK + s * kKVBytes, vdst = sbase + kOffV + s * kKVBytes;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar.k_full + s, kKVBytes + (uint32_t)(p.T * 8));
-                    bulk_load(sbase + kOffMask + s * 256, masks + c * p.T, (uint32_t)(p.T * 8), bar.k_full + s);
-                    mbar_arrive_expect_tx(bar.v_full + s, kKVBytes);
-                }
-                __syncwarp();
-                if (run) {
-                    if (lane == 0) {
-                        for (int kb = 0; kb < 4; ++kb)
-                            tma_load_2d(kdst + kb * (kKVBytes / 4), &maps.k_run, bar.k_full + s, kb * 64, first);
-                        for (int kb = 0; kb < 4; ++kb)
-                            tma_load_2d(vdst + kb * (kKVBytes / 4), &maps.v_run, bar.v_full + s, kb * 64, first);
+                int first = 0;
+                bool run = false;
+                if (c < it.nch) {
+                    const int64_t gk = gc + c;
+                    const int sk = (int)(gk % kStages);
+                    if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
+                    first = __shfl_sync(0xffffffffu, kk.x, 0);
+                    const int last = __shfl_sync(0xffffffffu, kk.w, 15);
+                    run = last - first == kChunkKeys - 1;  // ascending distinct keys: a contiguous run
+                    if (gk >= kStages && !wait(bar.k_empty + sk, gk / kStages - 1)) {
+                        ok = false;
+                        break;
                     }
-                } else if (lane < 16) {
-                    for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(kdst + lane * 512 + kb * (kKVBytes / 4), &maps.k_rows, bar.k_full + s, kb * 64,
-                                    kk.x, kk.y, kk.z, kk.w);
-                    for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(vdst + lane * 512 + kb * (kKVBytes / 4), &maps.v_rows, bar.v_full + s, kb * 64,
-                                    kk.x, kk.y, kk.z, kk.w);
+                    if (lane == 0) mbar_arrive_expect_tx(bar.k_full + sk, kKVBytes);
+                    __syncwarp();
+                    load_chunk_rows(sbase + kOffK + sk * kKVBytes, &maps.k_run, &maps.k_rows, bar.k_full + sk, run,
+                                    first, kk, lane);
+                    __syncwarp();
+                    last_k[sk] = gk;
                 }
-                __syncwarp();
-                last_gc[s] = gc;
+                if (c > 0) {
+                    const int64_t gv = gc + c - 1;
+                    const int sv = (int)(gv % kStages);
+                    if (gv >= kStages && !wait(bar.v_empty + sv, gv / kStages - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_expect_tx(bar.v_full + sv, kKVBytes);
+                    __syncwarp();
+                    load_chunk_rows(sbase + kOffV + sv * kKVBytes, &maps.v_run, &maps.v_rows, bar.v_full + sv, run_prev,
+                                    first_prev, kk_prev, lane);
+                    __syncwarp();
+                    last_v[sv] = gv;
+                }
+                kk_prev = kk;
+                first_prev = first;
+                run_prev = run;
             }
-            if (!ok) break;
+            gc += it.nch;
         }
+        if (!ok && lane == 0) fail(kSiteTileFwdWait, 1);
         // Drain: every issued copy must have landed before the CTA leaves.
         if (lane == 0) {
-            const int zero = 0;
             bool drained = true;
-            for (int i = 0; i < kStages; ++i)
-                if (last_gc[i] >= 0) {
-                    const uint32_t par = (uint32_t)((last_gc[i] / kStages) & 1);
-                    drained &= mbar_wait(bar.k_full + i, par, &zero, kWaitLimitNs);
-                    drained &= mbar_wait(bar.v_full + i, par, &zero, kWaitLimitNs);
-                }
+            for (int i = 0; i < kStages; ++i) {
+                if (last_k[i] >= 0)
+                    drained &= mbar_wait(bar.k_full + i, (uint32_t)((last_k[i] / kStages) & 1), &zero, kWaitLimitNs);
+                if (last_v[i] >= 0)
+                    drained &= mbar_wait(bar.v_full + i, (uint32_t)((last_v[i] / kStages) & 1), &zero, kWaitLimitNs);
+            }
             if (qc > 0) drained &= mbar_wait(bar.q_full, (uint32_t)((qc - 1) & 1), &zero, kWaitLimitNs);
             if (!drained) fail(kSiteTileFwdWait, 5);
         }
         __syncwarp();
     } else if (warp == 5) {
         // ---------------- MMA issuer ----------------
+        // Order per item: S(0), S(1), then PV(c), S(c+2) for each c.  S runs two chunks ahead so the
+        // softmax warps find S ready when they finish a chunk; PV(c) goes out as soon as P(c) is.
         constexpr uint32_t idesc_qk = idesc_bf16(kTileRows, kChunkKeys, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16(kTileRows, kHeadDim, false, true);
         int64_t gc = 0, qc = 0;
         Item it;
         bool ok = true;
+        auto issue_s = [&](int64_t g2) -> bool {
+            const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
+            if (!wait(bar.k_full + s, g2 / kStages)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + s * kKVBytes;
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = sdesc_sw128(qa + kb * (kQBytes / 4) + k * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(ka + kb * (kKVBytes / 4) + k * 32, 16, 1024);
+                        mma_bf16(tmem + kTmemS + sb * kChunkKeys, ad, bd, idesc_qk, (kb | k) ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar.s_full + sb);
+                mma_commit(bar.k_empty + s);
+            }
+            __syncwarp();
+            return true;
+        };
         auto issue_pv = [&](int64_t g2, bool first) -> bool {
             const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
-            if (!mbar_wait_warp(bar.p_full + sb, (g2 >> 1) & 1, abort_flag, p.wait_limit_ns)) return false;
-            if (!mbar_wait_warp(bar.v_full + s, (g2 / kStages) & 1, abort_flag, p.wait_limit_ns)) return false;
-            if (first && qc > 0 && !mbar_wait_warp(bar.o_free, (qc - 1) & 1, abort_flag, p.wait_limit_ns)) return false;
+            if (!wait(bar.p_full + sb, g2 >> 1)) return false;
+            if (!wait(bar.v_full + s, g2 / kStages)) return false;
+            if (first && qc > 0 && !wait(bar.o_free, qc - 1)) return false;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t pa = sbase + kOffP + sb * kPBytes;
@@ -262,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     const uint64_t bd = sdesc_sw128(va + k * 2048, kKVBytes / 4, 1024);
                     mma_bf16(tmem + kTmemO, ad, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
                 }
-                mma_commit(bar.kv_empty + s);
+                mma_commit(bar.v_empty + s);
                 mma_commit(bar.o_ready);
             }
             __syncwarp();
@@ -270,50 +324,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         };
         for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
-            if (!mbar_wait_warp(bar.q_full, qc & 1, abort_flag, p.wait_limit_ns)) {
+            if (!wait(bar.q_full, qc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            for (int c = 0; c < it.nch; ++c, ++gc) {
-                const int s = (int)(gc % kStages), sb = (int)(gc & 1);
-                if (!mbar_wait_warp(bar.k_full + s, (gc / kStages) & 1, abort_flag, p.wait_limit_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + s * kKVBytes;
-#pragma unroll
-                    for (int kb = 0; kb < 4; ++kb) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t ad = sdesc_sw128(qa + kb * (kQBytes / 4) + k * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(ka + kb * (kKVBytes / 4) + k * 32, 16, 1024);
-                            mma_bf16(tmem + kTmemS + sb * kChunkKeys, ad, bd, idesc_qk, (kb | k) ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(bar.s_full + sb);
-                }
-                __syncwarp();
-                if (c > 0 && !issue_pv(gc - 1, c == 1)) {
-                    ok = false;
-                    break;
-                }
+            for (int c = 0; ok && c < it.nch && c < 2; ++c) ok = issue_s(gc + c);
+            for (int c = 0; ok && c < it.nch; ++c) {
+                ok = issue_pv(gc + c, c == 0);
+                if (ok && c + 2 < it.nch) ok = issue_s(gc + c + 2);
             }
             if (!ok) break;
-            if (!issue_pv(gc - 1, it.nch == 1)) {
-                ok = false;
-                break;
-            }
             if (lane == 0) mma_commit(bar.q_empty);
             __syncwarp();
+            gc += it.nch;
             ++qc;
         }
         if (!ok && lane == 0) fail(kSiteTileFwdWait, 3);
         // Drain: all issued MMAs complete before the TMEM is released.
         if (lane == 0) {
-            const int zero = 0;
             mma_commit(bar.drain);
             if (!mbar_wait(bar.drain, 0, &zero, kWaitLimitNs)) fail(kSiteTileFwdWait, 6);
         }
@@ -339,16 +368,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 continue;
             }
+            const uint64_t *mrow = p.tile_masks + it.tile * p.max_chunks * p.T + qi;
+            uint64_t mask_next = __ldg(mrow);
             float m = -INFINITY, l = 0.f;
             for (int c = 0; c < it.nch; ++c, ++gc) {
-                const int s = (int)(gc % kStages), sb = (int)(gc & 1);
-                if (!mbar_wait_warp(bar.s_full + sb, (gc >> 1) & 1, abort_flag, p.wait_limit_ns) ||
-                    !mbar_wait_warp(bar.k_full + s, (gc / kStages) & 1, abort_flag, p.wait_limit_ns)) {
+                const int sb = (int)(gc & 1);
+                const uint64_t mask = mask_next;
+                if (c + 1 < it.nch) mask_next = __ldg(mrow + (c + 1) * p.T);
+                if (!wait(bar.s_full + sb, gc >> 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t mask = reinterpret_cast<const uint64_t *>(smem + kOffMask + s * 256)[qi];
                 uint32_t sr[2][32];
                 tmem_ld32(trow + kTmemS + sb * kChunkKeys, sr[0]);
                 tmem_ld32(trow + kTmemS + sb * kChunkKeys + 32, sr[1]);
@@ -368,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 bool prev_pv_seen = (c == 0);
                 if (__any_sync(0xffffffffu, need)) {
                     // Rescale O: the previous chunk's PV must have landed in TMEM first.
-                    if (!mbar_wait_warp(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, p.wait_limit_ns)) {
+                    if (!wait(bar.o_ready, gc - 1)) {
                         ok = false;
                         break;
                     }
@@ -407,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     *reinterpret_cast<uint4 *>(prow + phys * 16) =
                         make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
                 }
-                if (!prev_pv_seen && !mbar_wait_warp(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, p.wait_limit_ns)) {
+                if (!prev_pv_seen && !wait(bar.o_ready, gc - 1)) {
                     ok = false;
                     break;
                 }
@@ -417,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             }
             if (!ok) break;
             // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)) once the item's last PV has landed.
-            if (!mbar_wait_warp(bar.o_ready, (uint32_t)((gc - 1) & 1), abort_flag, p.wait_limit_ns)) {
+            if (!wait(bar.o_ready, gc - 1)) {
                 ok = false;
                 break;
             }
