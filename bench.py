@@ -427,7 +427,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=1, help="workload index (1 = the headline configuration)")
-    ap.add_argument("--cpu-rows", type=int, default=3072, help="query rows in the CPU-baseline oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=6144, help="query rows in the CPU-baseline oracle sample")
     ap.add_argument("--ref-rows", type=int, default=160, help="query rows per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
