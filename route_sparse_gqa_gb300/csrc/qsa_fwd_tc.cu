@@ -9,31 +9,38 @@
 //   producer warp   loads the chunk's 64 K rows and 64 V rows of head g into
 //                   128-byte-swizzled shared memory: four 64-row TMA tile boxes
 //                   when the keys form one contiguous run, otherwise TMA
-//                   tile::gather4 (four arbitrary rows per instruction);
-//   MMA warp        S = Q K^T (M=128, N=64, K=256) into TMEM, later
-//                   O += P V (M=128, N=256, K=64) into a TMEM accumulator;
-//   softmax warps   (4 warps, thread i owns TMEM lane / row i) read S, apply
-//                   the row's membership bits (read from global memory one
-//                   chunk ahead), run the online softmax in fp32 (base-2,
-//                   scale folded in, lazy rescale of O when the running max
-//                   grows by more than 2^8), write P as BF16 into shared memory
-//                   for the PV MMA, and finally normalise O, store it as BF16
-//                   and write LSE (natural log).
+//                   tile::gather4 (four arbitrary rows per instruction); it also
+//                   prefetches the next item's Q tile into L2;
+//   MMA warp        S = Q K^T (M=128, N=64, K=256) into TMEM with Q as the A
+//                   operand in TMEM, and O += P V (M=128, N=256, K=64) into a
+//                   TMEM accumulator with P as the A operand in TMEM -- shared
+//                   memory only feeds the B operands (K, V);
+//   softmax warps   (4 warps, thread i owns TMEM lane / row i) copy each item's
+//                   Q rows from global memory into TMEM, read S, apply the
+//                   row's membership bits (read from global memory one chunk
+//                   ahead), run the online softmax in fp32 (base-2, scale
+//                   folded in, lazy rescale of O when the running max grows by
+//                   more than 2^8), write P as BF16 into TMEM over the S buffer
+//                   it came from, and finally normalise O, store it as BF16 and
+//                   write LSE (natural log).
 //
 // Every K/V row gathered once into shared memory serves all G heads of the
 // group and all T queries of the tile that route to it.  Keys a query does not
 // route to get P = 0 exactly, so the result is the exact route-set softmax.
 //
-// Pipelining: K and V have separate two-stage rings.  A K stage is released as
-// soon as its S MMA completes and a V stage when its PV MMA completes; the
-// producer loads K of chunk c alongside V of chunk c-1, and the MMA warp keeps
-// S two chunks ahead of PV (order S0 S1 PV0 S2 PV1 S3 ...), so neither the
-// gather latency nor the PV waits sit on the softmax's critical path.  Two S
-// buffers in TMEM and two P buffers in shared memory alternate by chunk.  Every
-// mbarrier phase is consumed in order by each waiter, every wait is bounded in
-// time; on timeout the kernel records QSA_ERR_TIMEOUT in the workspace status
-// word, all roles wind down, in-flight copies and MMAs drain, the TMEM is freed
-// and the kernel returns.
+// TMEM (512 columns): O 0-255 (fp32), Q 256-383 (bf16 pairs), two S/P buffers
+// 384-447 and 448-511.  Shared memory: three-stage K and V rings (192 KiB).
+//
+// Pipelining: a K stage is released as soon as its S MMA completes and a V
+// stage when its PV MMA completes; the producer loads K of chunk c together
+// with V of chunk c-1, and the MMA warp keeps S two chunks ahead of PV (order
+// S0 S1 PV0 S2 PV1 S3 ...).  At the end of an item the softmax warps load the
+// next item's Q into TMEM (once the last S has read the current one) before the
+// epilogue, so the next item's S MMAs overlap it.  Every mbarrier phase is
+// consumed in order by each waiter and every wait is bounded in time; on
+// timeout the kernel records QSA_ERR_TIMEOUT in the workspace status word, all
+// roles wind down, in-flight copies and MMAs drain, the TMEM is freed and the
+// kernel returns.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -46,30 +53,28 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
 constexpr int kMaxPairs = kMaxKVPairs;  // (b, g) tensor-map sets per launch
-constexpr uint32_t kQBytes = kTileRows * kHeadDim * 2;       // 64 KiB
-constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;     // 32 KiB per K or V chunk
-constexpr uint32_t kPBytes = kTileRows * kChunkKeys * 2;     // 16 KiB
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;  // 32 KiB per K or V chunk
+constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kKVBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
-constexpr uint32_t kNumBars = 5 + 4 * kStages + 2 * 2;
+constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
+constexpr uint32_t kNumBars = 7 + 4 * kStages + 2 * 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0, kTmemS = 256;
+constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemSP = 384;  // S/P buffer b at kTmemSP + 64 b
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct FwdParams {
-    CUtensorMap q_map;                  // 4-D {D, Hq, S_q, B}, box {64, G, T, 1}
-    KVMaps kv[kMaxPairs];               // per (b, g): K/V row-gather and 64-row-run maps
+    CUtensorMap q_map;  // 4-D {D, Hq, S_q, B}, box {64, G, T, 1}: L2 prefetch of Q tiles
+    KVMaps kv[kMaxPairs];  // per (b, g): K/V row-gather and 64-row-run maps
+    const __nv_bfloat16 *q;
+    int64_t qs0, qs1, qs2;
     int64_t B, S_q, Hq, G, T, n_tiles, max_chunks;
     int64_t g0, n_g;   // KV heads handled by this launch
     int64_t n_items;   // n_g * B * n_tiles
@@ -103,7 +108,7 @@ __device__ __forceinline__ bool item_at(const FwdParams &p, int64_t round, Item 
 }
 
 struct Bars {
-    uint64_t *q_full, *q_empty, *o_ready, *o_free, *drain;
+    uint64_t *q_ready, *q_free, *o_ready, *o_free, *drain;
     uint64_t *k_full, *k_empty, *v_full, *v_empty;  // [kStages] each
     uint64_t *s_full, *p_full;                      // [2]
 };
@@ -111,17 +116,17 @@ struct Bars {
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + kOffBar);
     Bars r;
-    r.q_full = b + 0;
-    r.q_empty = b + 1;
+    r.q_ready = b + 0;
+    r.q_free = b + 1;
     r.o_ready = b + 2;
     r.o_free = b + 3;
     r.drain = b + 4;
-    r.k_full = b + 5;
-    r.k_empty = b + 5 + kStages;
-    r.v_full = b + 5 + 2 * kStages;
-    r.v_empty = b + 5 + 3 * kStages;
-    r.s_full = b + 5 + 4 * kStages;
-    r.p_full = b + 5 + 4 * kStages + 2;
+    r.k_full = b + 7;
+    r.k_empty = b + 7 + kStages;
+    r.v_full = b + 7 + 2 * kStages;
+    r.v_empty = b + 7 + 3 * kStages;
+    r.s_full = b + 7 + 4 * kStages;
+    r.p_full = b + 7 + 4 * kStages + 2;
     return r;
 }
 
@@ -138,6 +143,29 @@ __device__ __forceinline__ void load_chunk_rows(uint32_t dst, const CUtensorMap 
     }
 }
 
+// Thread r of the softmax warps copies its Q row (256 BF16) into TMEM lane r,
+// columns kTmemQ..kTmemQ+127 (column j holds elements 2j and 2j+1).  Rows past
+// S_q get zeros.
+__device__ __forceinline__ void load_q_row(const FwdParams &p, const Item &it, int qi, int hl, uint32_t trow) {
+    const int64_t q = it.t * p.T + qi;
+    const bool live = q < p.S_q;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.q + it.b * p.qs0 + q * p.qs1 + (it.g * p.G + hl) * p.qs2);
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 v = live ? __ldg(src + blk * 8 + i) : make_uint4(0, 0, 0, 0);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        tmem_st32(trow + kTmemQ + blk * 32, w);
+    }
+    tmem_st_wait();
+}
+
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -148,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const uint32_t sbase = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar.q_full, 1);
-        mbar_init(bar.q_empty, 1);
+        mbar_init(bar.q_ready, 128);
+        mbar_init(bar.q_free, 1);
         mbar_init(bar.o_ready, 1);
         mbar_init(bar.o_free, 128);
         mbar_init(bar.drain, 1);
@@ -170,9 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
-        prefetch_tmap(&p.q_map);
-    }
+    if (warp == 4 && lane == 0) prefetch_tmap(&p.q_map);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -189,26 +215,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 
     if (warp == 4) {
         // ---------------- producer ----------------
-        // K rows of chunk c are loaded one step ahead of the V rows of chunk c-1: S needs K
-        // early, PV needs V only after the softmax.  K and V have separate two-stage rings,
-        // released by S and by PV respectively.
-        int64_t gc = 0, qc = 0;
-        int64_t last_k[kStages] = {-1, -1}, last_v[kStages] = {-1, -1};
-        Item it;
+        int64_t gc = 0;
+        int64_t last_k[kStages], last_v[kStages];
+        for (int i = 0; i < kStages; ++i) last_k[i] = last_v[i] = -1;
+        Item it, nx;
         bool ok = true;
         for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
-            if (qc > 0 && !wait(bar.q_empty, qc - 1)) {
-                ok = false;
-                break;
-            }
+            // Warm L2 with the next non-empty item's Q tile while this one streams.
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar.q_full, kQBytes);
-                for (int kb = 0; kb < 4; ++kb)
-                    tma_load_4d(sbase + kOffQ + kb * (kQBytes / 4), &p.q_map, bar.q_full, kb * 64, (int)(it.g * p.G),
-                                (int)(it.t * p.T), (int)it.b);
+                for (int64_t r2 = round + 1; item_at(p, r2, nx); ++r2)
+                    if (nx.nch > 0) {
+                        for (int kb = 0; kb < 4; ++kb)
+                            tma_prefetch_4d(&p.q_map, kb * 64, (int)(nx.g * p.G), (int)(nx.t * p.T), (int)nx.b);
+                        break;
+                    }
             }
-            ++qc;
             const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
             const KVMaps &maps = p.kv[pair];
             const int32_t *keys = p.tile_keys + it.tile * p.max_chunks * kChunkKeys;
@@ -267,7 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 if (last_v[i] >= 0)
                     drained &= mbar_wait(bar.v_full + i, (uint32_t)((last_v[i] / kStages) & 1), &zero, kWaitLimitNs);
             }
-            if (qc > 0) drained &= mbar_wait(bar.q_full, (uint32_t)((qc - 1) & 1), &zero, kWaitLimitNs);
             if (!drained) fail(kSiteTileFwdWait, 5);
         }
         __syncwarp();
@@ -280,23 +301,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         int64_t gc = 0, qc = 0;
         Item it;
         bool ok = true;
-        auto issue_s = [&](int64_t g2) -> bool {
+        auto issue_s = [&](int64_t g2, bool last_s) -> bool {
             const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
             if (!wait(bar.k_full + s, g2 / kStages)) return false;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t qa = sbase + kOffQ, ka = sbase + kOffK + s * kKVBytes;
+                const uint32_t ka = sbase + kOffK + s * kKVBytes;
+                const uint32_t sp = tmem + kTmemSP + sb * kChunkKeys;
 #pragma unroll
                 for (int kb = 0; kb < 4; ++kb) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t ad = sdesc_sw128(qa + kb * (kQBytes / 4) + k * 32, 16, 1024);
                         const uint64_t bd = sdesc_sw128(ka + kb * (kKVBytes / 4) + k * 32, 16, 1024);
-                        mma_bf16(tmem + kTmemS + sb * kChunkKeys, ad, bd, idesc_qk, (kb | k) ? 1u : 0u);
+                        mma_bf16_ts(sp, tmem + kTmemQ + (kb * 4 + k) * 8, bd, idesc_qk, (kb | k) ? 1u : 0u);
                     }
                 }
                 mma_commit(bar.s_full + sb);
                 mma_commit(bar.k_empty + s);
+                if (last_s) mma_commit(bar.q_free);  // the item's Q in TMEM is no longer read
             }
             __syncwarp();
             return true;
@@ -308,13 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             if (first && qc > 0 && !wait(bar.o_free, qc - 1)) return false;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t pa = sbase + kOffP + sb * kPBytes;
                 const uint32_t va = sbase + kOffV + s * kKVBytes;
+                const uint32_t pa = tmem + kTmemSP + sb * kChunkKeys;
 #pragma unroll
                 for (int k = 0; k < kChunkKeys / 16; ++k) {
-                    const uint64_t ad = sdesc_sw128(pa + k * 32, 16, 1024);
                     const uint64_t bd = sdesc_sw128(va + k * 2048, kKVBytes / 4, 1024);
-                    mma_bf16(tmem + kTmemO, ad, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+                    mma_bf16_ts(tmem + kTmemO, pa + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
                 }
                 mma_commit(bar.v_empty + s);
                 mma_commit(bar.o_ready);
@@ -324,20 +345,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         };
         for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             if (it.nch == 0) continue;
-            if (!wait(bar.q_full, qc)) {
+            if (!wait(bar.q_ready, qc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            for (int c = 0; ok && c < it.nch && c < 2; ++c) ok = issue_s(gc + c);
-            for (int c = 0; ok && c < it.nch; ++c) {
+            const int n = it.nch;
+            for (int c = 0; ok && c < n && c < 2; ++c) ok = issue_s(gc + c, c == n - 1);
+            for (int c = 0; ok && c < n; ++c) {
                 ok = issue_pv(gc + c, c == 0);
-                if (ok && c + 2 < it.nch) ok = issue_s(gc + c + 2);
+                if (ok && c + 2 < n) ok = issue_s(gc + c + 2, c + 2 == n - 1);
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(bar.q_empty);
-            __syncwarp();
-            gc += it.nch;
+            gc += n;
             ++qc;
         }
         if (!ok && lane == 0) fail(kSiteTileFwdWait, 3);
@@ -348,13 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
         __syncwarp();
     } else {
-        // ---------------- softmax / epilogue (warps 0-3) ----------------
+        // ---------------- softmax / Q loader / epilogue (warps 0-3) ----------------
         const int r = threadIdx.x;  // row of the tile = TMEM lane
         const int qi = (int)(r / p.G), hl = (int)(r % p.G);
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         int64_t gc = 0, qc = 0;
         Item it;
         bool ok = true;
+        bool have_q = false;  // Q of the current item is already in TMEM
         for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
             const int64_t q = it.t * p.T + qi;
             const int64_t h = it.g * p.G + hl;
@@ -368,11 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 continue;
             }
+            if (!have_q) {  // only for the first non-empty item; later ones are loaded ahead
+                load_q_row(p, it, qi, hl, trow);
+                tc_fence_before();
+                mbar_arrive(bar.q_ready);
+            }
             const uint64_t *mrow = p.tile_masks + it.tile * p.max_chunks * p.T + qi;
             uint64_t mask_next = __ldg(mrow);
             float m = -INFINITY, l = 0.f;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 const int sb = (int)(gc & 1);
+                const uint32_t sp = trow + kTmemSP + sb * kChunkKeys;
                 const uint64_t mask = mask_next;
                 if (c + 1 < it.nch) mask_next = __ldg(mrow + (c + 1) * p.T);
                 if (!wait(bar.s_full + sb, gc >> 1)) {
@@ -381,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 uint32_t sr[2][32];
-                tmem_ld32(trow + kTmemS + sb * kChunkKeys, sr[0]);
-                tmem_ld32(trow + kTmemS + sb * kChunkKeys + 32, sr[1]);
+                tmem_ld32(sp, sr[0]);
+                tmem_ld32(sp + 32, sr[1]);
                 tmem_ld_wait();
                 float x[64];
                 float mx = -INFINITY;
@@ -431,20 +458,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     pk[j >> 1] = pack_bf16(p0, p1);
                 }
                 l += lsum;
-                uint8_t *prow = smem + kOffP + sb * kPBytes + r * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const int phys = ch ^ (r & 7);
-                    *reinterpret_cast<uint4 *>(prow + phys * 16) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                }
+                tmem_st32(sp, pk);  // P over the first half of the S buffer it came from
+                tmem_st_wait();
                 if (!prev_pv_seen && !wait(bar.o_ready, gc - 1)) {
                     ok = false;
                     break;
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar.p_full + sb);
+            }
+            if (!ok) break;
+            // Load the next non-empty item's Q once this item's last S has read the current one, so the
+            // MMA warp can start it while this epilogue runs.
+            have_q = false;
+            Item nx;
+            for (int64_t r2 = round + 1; item_at(p, r2, nx); ++r2) {
+                if (nx.nch == 0) continue;
+                if (!wait(bar.q_free, qc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                load_q_row(p, nx, qi, hl, trow);
+                tc_fence_before();
+                mbar_arrive(bar.q_ready);
+                have_q = true;
+                break;
             }
             if (!ok) break;
             // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)) once the item's last PV has landed.
@@ -504,6 +543,10 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
     }
     const int sms = tc_num_sms();
     const int64_t g_per_launch = std::max<int64_t>(1, kMaxPairs / a.B);
+    p.q = a.q;
+    p.qs0 = a.qs0;
+    p.qs1 = a.qs1;
+    p.qs2 = a.qs2;
     p.B = a.B;
     p.S_q = a.S_q;
     p.Hq = a.Hq;
