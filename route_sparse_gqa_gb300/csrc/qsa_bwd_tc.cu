@@ -413,7 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             float *dk_base = p.dk_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
             float *dv_base = p.dv_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
             for (int c = 0; c < it.nch; ++c, ++gc) {
+                // The chunk's 64 keys, one pair per lane, broadcast below with shuffles.  The loop has no
+                // branch: a partial chunk's padding columns have empty membership, so their dK^T/dV^T
+                // columns are exact zeros and adding them to the padding key's row changes nothing.
+                // Branch-free, the key broadcasts do not wait on one another and the reductions issue
+                // back to back.
                 const int32_t *keys = p.tile_keys + (it.tile * p.max_chunks + c) * kChunkKeys;
+                const int32_t key_lo = __ldg(keys + lane), key_hi = __ldg(keys + 32 + lane);
                 for (int h = 0; h < 2; ++h, ++u) {
                     if (!wait(kGradsFull, u)) {
                         ok = false;
@@ -428,16 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     tmem_ld_wait();
                     tc_fence_before();
                     mbar_arrive(bars + kFlushDone);
-                    int32_t prev = -1;
 #pragma unroll
                     for (int j = 0; j < 64; ++j) {
-                        const int32_t key = __ldg(keys + j);
-                        if (key > prev) {  // keys ascend; the padding of a partial chunk repeats an earlier key
-                            const int64_t off = (int64_t)key * row_stride + h * 128;
-                            atomicAdd(dk_base + off, __uint_as_float(a[j >> 5][j & 31]));
-                            atomicAdd(dv_base + off, __uint_as_float(v[j >> 5][j & 31]));
-                            prev = key;
-                        }
+                        const int32_t key = __shfl_sync(0xffffffffu, j < 32 ? key_lo : key_hi, j & 31);
+                        const int64_t off = (int64_t)key * row_stride + h * 128;
+                        red_add_f32(dk_base + off, __uint_as_float(a[j >> 5][j & 31]));
+                        red_add_f32(dv_base + off, __uint_as_float(v[j >> 5][j & 31]));
                     }
                 }
                 if (!ok) break;

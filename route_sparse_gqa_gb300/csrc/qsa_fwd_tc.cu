@@ -31,16 +31,22 @@
 // TMEM (512 columns): O 0-255 (fp32), Q 256-383 (bf16 pairs), two S/P buffers
 // 384-447 and 448-511.  Shared memory: three-stage K and V rings (192 KiB).
 //
-// Pipelining: a K stage is released as soon as its S MMA completes and a V
-// stage when its PV MMA completes; the producer loads K of chunk c together
-// with V of chunk c-1, and the MMA warp keeps S two chunks ahead of PV (order
-// S0 S1 PV0 S2 PV1 S3 ...).  At the end of an item the softmax warps load the
-// next item's Q into TMEM (once the last S has read the current one) before the
-// epilogue, so the next item's S MMAs overlap it.  Every mbarrier phase is
-// consumed in order by each waiter and every wait is bounded in time; on
-// timeout the kernel records QSA_ERR_TIMEOUT in the workspace status word, all
-// roles wind down, in-flight copies and MMAs drain, the TMEM is freed and the
-// kernel returns.
+// Pipelining: every per-chunk barrier is indexed by the chunk's stage (global
+// chunk number mod 3).  A K stage is reused once the S MMA that read it has
+// completed (the barrier that tells the softmax warps S is ready), a V stage
+// once its PV MMA has (the barrier that tells them O is current); the producer
+// loads K of chunk c together with V of chunk c-1.  One thread issues every
+// MMA, S two chunks ahead of PV (S0 S1 PV0 S2 PV1 S3 ...), and takes the
+// waits for each PV(c), S(c+2) pair back to back: a waiting thread stalls
+// until the tensor pipe has taken its queued MMAs, so a wait between the two
+// groups would leave the pipe idle.  At the end of an item the softmax warps
+// load the next item's Q into TMEM (once the last S has read the current one)
+// before the epilogue, so the next item's S MMAs overlap it.  A parity wait
+// is unambiguous only if the waited phase is the barrier's open one or the one
+// just completed; each wait below states why that holds.  Every wait is
+// bounded in time; on timeout the kernel records QSA_ERR_TIMEOUT in the
+// workspace status word, all roles wind down, in-flight copies and MMAs drain,
+// the TMEM is freed and the kernel returns.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -60,7 +66,7 @@ constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;  // 32 KiB per K or V c
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
 constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
-constexpr uint32_t kNumBars = 7 + 4 * kStages + 2 * 2;
+constexpr uint32_t kNumBars = 5 + 5 * kStages;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
@@ -107,10 +113,14 @@ __device__ __forceinline__ bool item_at(const FwdParams &p, int64_t round, Item 
     return true;
 }
 
+// Per-chunk barriers are indexed by the global chunk number c modulo kStages
+// (the K/V stage of chunk c); the S/P TMEM buffer of chunk c is c % 2.
 struct Bars {
-    uint64_t *q_ready, *q_free, *o_ready, *o_free, *drain;
-    uint64_t *k_full, *k_empty, *v_full, *v_empty;  // [kStages] each
-    uint64_t *s_full, *p_full;                      // [2]
+    uint64_t *q_ready, *q_free, *o_free, *drain;
+    uint64_t *k_full, *v_full;  // copies of chunk c landed (TMA transaction bytes)
+    uint64_t *s_full;           // S(c) complete: softmax may read it, K stage reusable
+    uint64_t *p_full;           // P(c) written by the 128 softmax threads
+    uint64_t *o_ready;          // PV(c) complete: V stage reusable, O current up to c
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
@@ -118,15 +128,13 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     Bars r;
     r.q_ready = b + 0;
     r.q_free = b + 1;
-    r.o_ready = b + 2;
-    r.o_free = b + 3;
-    r.drain = b + 4;
-    r.k_full = b + 7;
-    r.k_empty = b + 7 + kStages;
-    r.v_full = b + 7 + 2 * kStages;
-    r.v_empty = b + 7 + 3 * kStages;
-    r.s_full = b + 7 + 4 * kStages;
-    r.p_full = b + 7 + 4 * kStages + 2;
+    r.o_free = b + 2;
+    r.drain = b + 3;
+    r.k_full = b + 5;
+    r.v_full = b + 5 + kStages;
+    r.s_full = b + 5 + 2 * kStages;
+    r.p_full = b + 5 + 3 * kStages;
+    r.o_ready = b + 5 + 4 * kStages;
     return r;
 }
 
@@ -178,18 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         mbar_init(bar.q_ready, 128);
         mbar_init(bar.q_free, 1);
-        mbar_init(bar.o_ready, 1);
         mbar_init(bar.o_free, 128);
         mbar_init(bar.drain, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar.k_full + s, 1);
-            mbar_init(bar.k_empty + s, 1);
             mbar_init(bar.v_full + s, 1);
-            mbar_init(bar.v_empty + s, 1);
-        }
-        for (int s = 0; s < 2; ++s) {
             mbar_init(bar.s_full + s, 1);
             mbar_init(bar.p_full + s, 128);
+            mbar_init(bar.o_ready + s, 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -248,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     first = __shfl_sync(0xffffffffu, kk.x, 0);
                     const int last = __shfl_sync(0xffffffffu, kk.w, 15);
                     run = last - first == kChunkKeys - 1;  // ascending distinct keys: a contiguous run
-                    if (gk >= kStages && !wait(bar.k_empty + sk, gk / kStages - 1)) {
+                    // The stage is free once S of chunk gk - kStages (which read it) has completed.
+                    if (gk >= kStages && !wait(bar.s_full + sk, gk / kStages - 1)) {
                         ok = false;
                         break;
                     }
@@ -262,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 if (c > 0) {
                     const int64_t gv = gc + c - 1;
                     const int sv = (int)(gv % kStages);
-                    if (gv >= kStages && !wait(bar.v_empty + sv, gv / kStages - 1)) {
+                    // ... and once PV of chunk gv - kStages has completed.
+                    if (gv >= kStages && !wait(bar.o_ready + sv, gv / kStages - 1)) {
                         ok = false;
                         break;
                     }
@@ -293,19 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
         __syncwarp();
     } else if (warp == 5) {
-        // ---------------- MMA issuer ----------------
-        // Order per item: S(0), S(1), then PV(c), S(c+2) for each c.  S runs two chunks ahead so the
-        // softmax warps find S ready when they finish a chunk; PV(c) goes out as soon as P(c) is.
-        constexpr uint32_t idesc_qk = idesc_bf16(kTileRows, kChunkKeys, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16(kTileRows, kHeadDim, false, true);
-        int64_t gc = 0, qc = 0;
-        Item it;
-        bool ok = true;
-        auto issue_s = [&](int64_t g2, bool last_s) -> bool {
-            const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
-            if (!wait(bar.k_full + s, g2 / kStages)) return false;
-            tc_fence_after();
-            if (lane == 0) {
+        // ---------------- MMA issuer (one thread) ----------------
+        // Order per item: S(0), S(1), then PV(c), S(c+2) for each c: S runs two chunks ahead so the
+        // softmax warps find S ready when they finish a chunk.  The issuing thread executes no
+        // warp-collective instruction and takes all waits for a PV(c), S(c+2) pair together: a
+        // wait (any shared-memory access) stalls the thread until its queued MMAs have been taken
+        // by the tensor pipe, so one wait per pair keeps that pipe fed.
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16(kTileRows, kChunkKeys, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(kTileRows, kHeadDim, false, true);
+            auto wait1 = [&](uint64_t *b, int64_t phase) {
+                return mbar_wait(b, (uint32_t)(phase & 1), abort_flag, p.wait_limit_ns);
+            };
+            auto issue_s = [&](int64_t g2, bool last_s) {
+                const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
                 const uint32_t ka = sbase + kOffK + s * kKVBytes;
                 const uint32_t sp = tmem + kTmemSP + sb * kChunkKeys;
 #pragma unroll
@@ -316,20 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         mma_bf16_ts(sp, tmem + kTmemQ + (kb * 4 + k) * 8, bd, idesc_qk, (kb | k) ? 1u : 0u);
                     }
                 }
-                mma_commit(bar.s_full + sb);
-                mma_commit(bar.k_empty + s);
+                mma_commit(bar.s_full + s);
                 if (last_s) mma_commit(bar.q_free);  // the item's Q in TMEM is no longer read
-            }
-            __syncwarp();
-            return true;
-        };
-        auto issue_pv = [&](int64_t g2, bool first) -> bool {
-            const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
-            if (!wait(bar.p_full + sb, g2 >> 1)) return false;
-            if (!wait(bar.v_full + s, g2 / kStages)) return false;
-            if (first && qc > 0 && !wait(bar.o_free, qc - 1)) return false;
-            tc_fence_after();
-            if (lane == 0) {
+            };
+            auto issue_pv = [&](int64_t g2, bool first) {
+                const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
                 const uint32_t va = sbase + kOffV + s * kKVBytes;
                 const uint32_t pa = tmem + kTmemSP + sb * kChunkKeys;
 #pragma unroll
@@ -337,32 +335,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     const uint64_t bd = sdesc_sw128(va + k * 2048, kKVBytes / 4, 1024);
                     mma_bf16_ts(tmem + kTmemO, pa + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
                 }
-                mma_commit(bar.v_empty + s);
-                mma_commit(bar.o_ready);
+                mma_commit(bar.o_ready + s);
+            };
+            int64_t gc = 0, qc = 0;
+            Item it;
+            bool ok = true;
+            for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+                if (it.nch == 0) continue;
+                const int n = it.nch;
+                ok = wait1(bar.q_ready, qc);
+                for (int c = 0; ok && c < n && c < 2; ++c) {
+                    ok = wait1(bar.k_full + (gc + c) % kStages, (gc + c) / kStages);
+                    tc_fence_after();
+                    if (ok) issue_s(gc + c, c == n - 1);
+                }
+                for (int c = 0; ok && c < n; ++c) {
+                    const int64_t g2 = gc + c;
+                    ok = wait1(bar.p_full + g2 % kStages, g2 / kStages) && wait1(bar.v_full + g2 % kStages, g2 / kStages) &&
+                         (c > 0 || qc == 0 || wait1(bar.o_free, qc - 1)) &&
+                         (c + 2 >= n || wait1(bar.k_full + (g2 + 2) % kStages, (g2 + 2) / kStages));
+                    tc_fence_after();
+                    if (!ok) break;
+                    issue_pv(g2, c == 0);
+                    if (c + 2 < n) issue_s(g2 + 2, c + 2 == n - 1);
+                }
+                gc += n;
+                ++qc;
             }
-            __syncwarp();
-            return true;
-        };
-        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
-            if (it.nch == 0) continue;
-            if (!wait(bar.q_ready, qc)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const int n = it.nch;
-            for (int c = 0; ok && c < n && c < 2; ++c) ok = issue_s(gc + c, c == n - 1);
-            for (int c = 0; ok && c < n; ++c) {
-                ok = issue_pv(gc + c, c == 0);
-                if (ok && c + 2 < n) ok = issue_s(gc + c + 2, c + 2 == n - 1);
-            }
-            if (!ok) break;
-            gc += n;
-            ++qc;
-        }
-        if (!ok && lane == 0) fail(kSiteTileFwdWait, 3);
-        // Drain: all issued MMAs complete before the TMEM is released.
-        if (lane == 0) {
+            if (!ok) fail(kSiteTileFwdWait, 3);
+            // Drain: all issued MMAs complete before the TMEM is released.
             mma_commit(bar.drain);
             if (!mbar_wait(bar.drain, 0, &zero, kWaitLimitNs)) fail(kSiteTileFwdWait, 6);
         }
@@ -398,11 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             uint64_t mask_next = __ldg(mrow);
             float m = -INFINITY, l = 0.f;
             for (int c = 0; c < it.nch; ++c, ++gc) {
-                const int sb = (int)(gc & 1);
+                const int sb = (int)(gc & 1), st = (int)(gc % kStages);
                 const uint32_t sp = trow + kTmemSP + sb * kChunkKeys;
                 const uint64_t mask = mask_next;
                 if (c + 1 < it.nch) mask_next = __ldg(mrow + (c + 1) * p.T);
-                if (!wait(bar.s_full + sb, gc >> 1)) {
+                if (!wait(bar.s_full + st, gc / kStages)) {
                     ok = false;
                     break;
                 }
@@ -420,17 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 const bool need = (m != -INFINITY) && (mx > m + kRescaleThreshold);
                 if (m == -INFINITY) m = mx;  // first keys of this row: nothing accumulated yet
-                // o_ready completes once per PV.  These warps consume every phase exactly once and in
-                // order (the PV of chunk c-1 during chunk c, the item's last PV in the epilogue), so a
-                // parity wait always targets the oldest open phase and is never ambiguous.
-                bool prev_pv_seen = (c == 0);
                 if (__any_sync(0xffffffffu, need)) {
-                    // Rescale O: the previous chunk's PV must have landed in TMEM first.
-                    if (!wait(bar.o_ready, gc - 1)) {
+                    // Rescale O: the previous chunk's PV must have landed in TMEM first.  S(c) is
+                    // complete, so every MMA issued before it is too, among them the PV three chunks
+                    // back that completed the previous phase of this barrier: the parity wait below
+                    // can only mean PV(c-1), and PV(c+2) cannot complete before P(c+2) exists.
+                    if (!wait(bar.o_ready + (gc - 1) % kStages, (gc - 1) / kStages)) {
                         ok = false;
                         break;
                     }
-                    prev_pv_seen = true;
                     tc_fence_after();
                     const float alpha = need ? ex2(m - mx) : 1.f;
 #pragma unroll 1
@@ -460,12 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 l += lsum;
                 tmem_st32(sp, pk);  // P over the first half of the S buffer it came from
                 tmem_st_wait();
-                if (!prev_pv_seen && !wait(bar.o_ready, gc - 1)) {
-                    ok = false;
-                    break;
-                }
                 tc_fence_before();
-                mbar_arrive(bar.p_full + sb);
+                mbar_arrive(bar.p_full + st);
             }
             if (!ok) break;
             // Load the next non-empty item's Q once this item's last S has read the current one, so the
@@ -487,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             }
             if (!ok) break;
             // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)) once the item's last PV has landed.
-            if (!wait(bar.o_ready, gc - 1)) {
+            if (!wait(bar.o_ready + (gc - 1) % kStages, (gc - 1) / kStages)) {
                 ok = false;
                 break;
             }

@@ -82,6 +82,13 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, c
     return __all_sync(0xffffffffu, ok);
 }
 
+// ---- global reductions ----
+// Relaxed fp32 add into global memory without a returned value (a reduction,
+// not an atomic read-modify-write visible to the issuing thread).
+__device__ __forceinline__ void red_add_f32(float *addr, float v) {
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
 // ---- TMA ----
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
