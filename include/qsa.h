@@ -88,8 +88,10 @@ QSA_API qsa_status qsa_check_problem(const qsa_problem *problem);
  * this problem (256-byte aligned base required), or 0 if the problem is
  * invalid.  The workspace holds the preprocessed routes (per-row sorted unique
  * IDs and counts, per-tile key lists and membership masks, the work order),
- * the backward pass's fp32 row statistics and dK/dV accumulators, and a device
- * status word. */
+ * the backward pass's fp32 row statistics and dK/dV accumulators, the work
+ * queue counters of the attention kernels, and a device status word.  Every
+ * call that takes the workspace updates it, so calls sharing one workspace
+ * must be ordered (one stream, or events between streams). */
 QSA_API size_t qsa_workspace_bytes(const qsa_problem *problem);
 
 /* Route preprocessing (fa4_qsa _preprocess and _block_kinds/_compact_blocks
@@ -104,10 +106,11 @@ QSA_API qsa_status qsa_preprocess(const qsa_problem *problem, const void *routes
 
 /* Forward pass (flex_sparse_gqa_attention / fa4_sparse_gqa_attention returns O;
  * the per-row LSE is kept for the backward pass).  Needs a workspace filled by
- * qsa_preprocess for the same problem.  o and lse are written in full (rows
- * with no valid route get O = 0 and LSE = -inf); they must not overlap q, k, v
- * or the workspace. */
-QSA_API qsa_status qsa_forward(const qsa_problem *problem, const void *workspace, size_t ws_bytes, const void *q,
+ * qsa_preprocess for the same problem; the preprocessed routes are only read,
+ * the work queue counters are used and left reset.  o and lse are written in
+ * full (rows with no valid route get O = 0 and LSE = -inf); they must not
+ * overlap q, k, v or the workspace. */
+QSA_API qsa_status qsa_forward(const qsa_problem *problem, void *workspace, size_t ws_bytes, const void *q,
                        const void *k, const void *v, void *o, float *lse, cudaStream_t stream);
 
 /* First-order backward (fa4_sparse_gqa_attention: first-order autograd only,

@@ -72,6 +72,8 @@ Layout make_layout(const qsa_problem *p) {
     size_t off = 0;
     L.off_status = off;
     off = align256(off + sizeof(DeviceStatus));
+    L.off_sched = off;  // work queue counters of the tile kernels: {next, done} for forward, then backward
+    off = align256(off + 4 * sizeof(int32_t));
     L.off_counts = off;
     off = align256(off + rows * sizeof(int32_t));
     L.off_ids = off;
@@ -155,8 +157,9 @@ AttnArgs attn_args(const qsa_problem *p, const Layout &L, const void *ws, const 
     return a;
 }
 
-TileArgs tile_args(const qsa_problem *p, const Layout &L, const void *ws) {
+TileArgs tile_args(const qsa_problem *p, const Layout &L, void *ws) {
     TileArgs t{};
+    t.sched = at<int32_t>(ws, L.off_sched);
     t.T = L.T;
     t.n_tiles = L.n_tiles;
     t.max_chunks = L.max_chunks;
@@ -191,7 +194,8 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
     if (!routes) return fail(QSA_ERR_INVALID_ARGUMENT, "routes is null");
     if (reinterpret_cast<uintptr_t>(routes) % (p->route_bits / 8) != 0)
         return fail(QSA_ERR_INVALID_ARGUMENT, "routes pointer is not aligned to its element size");
-    cudaError_t e = cudaMemsetAsync(at<DeviceStatus>(ws, L.off_status), 0, sizeof(DeviceStatus), stream);
+    // Status word and work queue counters (the tile kernels leave the counters reset when they end).
+    cudaError_t e = cudaMemsetAsync(at<DeviceStatus>(ws, L.off_status), 0, L.off_counts - L.off_status, stream);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
     RowsArgs r{};
     r.routes = routes;
@@ -229,7 +233,7 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
     return QSA_OK;
 }
 
-qsa_status qsa_forward(const qsa_problem *p, const void *ws, size_t ws_bytes, const void *q, const void *k,
+qsa_status qsa_forward(const qsa_problem *p, void *ws, size_t ws_bytes, const void *q, const void *k,
                        const void *v, void *o, float *lse, cudaStream_t stream) {
     Layout L;
     qsa_status st = check_ws(p, ws, ws_bytes, L);

@@ -35,6 +35,7 @@
 
 #include "qsa_tc.cuh"
 #include "qsa_tc_ptx.cuh"
+#include "qsa_queue.cuh"
 
 namespace qsa {
 namespace {
@@ -53,7 +54,9 @@ constexpr uint32_t kOffV = kOffK + kKVBytes;
 constexpr uint32_t kOffP = kOffV + kKVBytes;
 constexpr uint32_t kOffDS = kOffP + kPBytes;
 constexpr uint32_t kOffBar = kOffDS + kPBytes;
-constexpr uint32_t kNumBars = 16;
+constexpr uint32_t kBarItemFull = 16;  // work queue ring: full [kQueueRing], then empty [kQueueRing]
+constexpr uint32_t kBarItemEmpty = kBarItemFull + kQueueRing;
+constexpr uint32_t kNumBars = kBarItemEmpty + kQueueRing;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -72,29 +75,14 @@ struct BwdParams {
     const int32_t *tile_keys;
     const uint64_t *tile_masks;
     const int32_t *order;
+    int32_t *sched;  // work queue counters {next, done}
     const float *lse, *delta;
     __nv_bfloat16 *dq;
     float *dk_acc, *dv_acc;
     DeviceStatus *status;
 };
 
-struct Item {
-    int64_t b, g, tile, t;
-    int nch;
-};
-
-__device__ __forceinline__ bool item_at(const BwdParams &p, int64_t round, Item &it) {
-    const int64_t grid = gridDim.x;
-    const int64_t idx = round * grid + ((round & 1) ? (grid - 1 - blockIdx.x) : blockIdx.x);
-    if (idx >= p.n_items) return false;
-    const int64_t per_g = p.B * p.n_tiles;
-    it.g = p.g0 + idx / per_g;
-    it.tile = p.order[idx % per_g];
-    it.b = it.tile / p.n_tiles;
-    it.t = it.tile % p.n_tiles;
-    it.nch = p.tile_nchunks[it.tile];
-    return true;
-}
+using Item = QueueItem;
 
 enum BarId {
     kQFull, kQEmpty, kKFull, kKEmpty, kVFull, kVEmpty, kSDFull, kPDSFull, kPDSEmpty, kGradsFull, kFlushDone,
@@ -107,12 +95,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + kOffMisc + 16);  // [kQueueRing]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
 
     if (threadIdx.x == 0) {
         const uint32_t counts[kDrain + 1] = {1, 1, 1, 1, 1, 1, 1, 128, 1, 1, 128, 1, 128, 1};
         for (int i = 0; i <= kDrain; ++i) mbar_init(bars + i, counts[i]);
+        for (int i = 0; i < kQueueRing; ++i) {
+            mbar_init(bars + kBarItemFull + i, 1);
+            mbar_init(bars + kBarItemEmpty + i, 32 + 128 + 128);  // MMA warp, softmax and flush threads take every item
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -143,7 +136,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int64_t gc = 0, qc = 0, v_issued = 0, k_issued = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+        for (int64_t pos = 0; ok; ++pos) {
+            int32_t idx = -1;
+            if (lane == 0) ok = queue_claim(p.sched, p.n_items, ring, bars + kBarItemFull, bars + kBarItemEmpty, pos,
+                                            abort_flag, p.wait_limit_ns, idx);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            if (!ok || idx < 0) break;
+            queue_decode(p, idx, it);
             if (it.nch == 0) continue;
             if (qc > 0 && !wait(kQEmpty, qc - 1)) {
                 ok = false;
@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             }
         }
         if (!ok && lane == 0) fail(1);
+        if (lane == 0) queue_finish(p.sched);
         // Drain every issued copy before the CTA can leave.
         if (lane == 0) {
             bool drained = true;
@@ -221,7 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int64_t gc = 0, qc = 0, u = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+        for (int64_t pos = 0; ok; ++pos) {
+            int32_t idx = -1;
+            ok = queue_take(ring, bars + kBarItemFull, bars + kBarItemEmpty, pos, abort_flag, p.wait_limit_ns, true, idx);
+            if (!ok || idx < 0) break;
+            queue_decode(p, idx, it);
             if (it.nch == 0) continue;
             if (!wait(kQFull, qc)) {
                 ok = false;
@@ -309,7 +314,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int64_t gc = 0, qc = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+        for (int64_t pos = 0; ok; ++pos) {
+            int32_t idx = -1;
+            ok = queue_take(ring, bars + kBarItemFull, bars + kBarItemEmpty, pos, abort_flag, p.wait_limit_ns, true, idx);
+            if (!ok || idx < 0) break;
+            queue_decode(p, idx, it);
             const int64_t q = it.t * p.T + qi;
             const int64_t h = it.g * p.G + hl;
             const bool live = q < p.S_q;
@@ -407,7 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int64_t gc = 0, u = 0;
         Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+        for (int64_t pos = 0; ok; ++pos) {
+            int32_t idx = -1;
+            ok = queue_take(ring, bars + kBarItemFull, bars + kBarItemEmpty, pos, abort_flag, p.wait_limit_ns, true, idx);
+            if (!ok || idx < 0) break;
+            queue_decode(p, idx, it);
             if (it.nch == 0) continue;
             const int64_t row_stride = p.Hkv * kHeadDim;
             float *dk_base = p.dk_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
@@ -495,6 +508,7 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
     p.tile_keys = t.tile_keys;
     p.tile_masks = t.tile_masks;
     p.order = t.order;
+    p.sched = t.sched + 2;  // backward counters
     p.lse = bw.lse;
     p.delta = bw.delta;
     p.dq = bw.dq;

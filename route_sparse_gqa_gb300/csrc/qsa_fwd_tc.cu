@@ -53,6 +53,7 @@
 
 #include "qsa_tc.cuh"
 #include "qsa_tc_ptx.cuh"
+#include "qsa_queue.cuh"
 
 namespace qsa {
 namespace {
@@ -66,7 +67,7 @@ constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;  // 32 KiB per K or V c
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
 constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
-constexpr uint32_t kNumBars = 5 + 5 * kStages;
+constexpr uint32_t kNumBars = 5 + 5 * kStages + 2 * kQueueRing;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
@@ -90,33 +91,19 @@ struct FwdParams {
     const int32_t *tile_keys;
     const uint64_t *tile_masks;
     const int32_t *order;
+    int32_t *sched;  // work queue counters {next, done}
     __nv_bfloat16 *o;
     float *lse;
     DeviceStatus *status;
 };
 
-struct Item {
-    int64_t b, g, tile, t;
-    int nch;
-};
-
-__device__ __forceinline__ bool item_at(const FwdParams &p, int64_t round, Item &it) {
-    const int64_t grid = gridDim.x;
-    const int64_t idx = round * grid + ((round & 1) ? (grid - 1 - blockIdx.x) : blockIdx.x);  // snake order
-    if (idx >= p.n_items) return false;
-    const int64_t per_g = p.B * p.n_tiles;
-    it.g = p.g0 + idx / per_g;
-    it.tile = p.order[idx % per_g];
-    it.b = it.tile / p.n_tiles;
-    it.t = it.tile % p.n_tiles;
-    it.nch = p.tile_nchunks[it.tile];
-    return true;
-}
+using Item = QueueItem;
 
 // Per-chunk barriers are indexed by the global chunk number c modulo kStages
 // (the K/V stage of chunk c); the S/P TMEM buffer of chunk c is c % 2.
 struct Bars {
     uint64_t *q_ready, *q_free, *o_free, *drain;
+    uint64_t *item_full, *item_empty;  // work queue ring [kQueueRing]
     uint64_t *k_full, *v_full;  // copies of chunk c landed (TMA transaction bytes)
     uint64_t *s_full;           // S(c) complete: softmax may read it, K stage reusable
     uint64_t *p_full;           // P(c) written by the 128 softmax threads
@@ -135,6 +122,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     r.s_full = b + 5 + 2 * kStages;
     r.p_full = b + 5 + 3 * kStages;
     r.o_ready = b + 5 + 4 * kStages;
+    r.item_full = b + 5 + 5 * kStages;
+    r.item_empty = r.item_full + kQueueRing;
     return r;
 }
 
@@ -180,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const Bars bar = bars_at(smem);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + kOffMisc + 16);  // [kQueueRing]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
 
@@ -194,6 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             mbar_init(bar.s_full + s, 1);
             mbar_init(bar.p_full + s, 128);
             mbar_init(bar.o_ready + s, 1);
+        }
+        for (int s = 0; s < kQueueRing; ++s) {
+            mbar_init(bar.item_full + s, 1);
+            mbar_init(bar.item_empty + s, 1 + 128);  // the MMA thread and the softmax threads take every item
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -222,19 +216,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         int64_t gc = 0;
         int64_t last_k[kStages], last_v[kStages];
         for (int i = 0; i < kStages; ++i) last_k[i] = last_v[i] = -1;
-        Item it, nx;
+        Item it;
         bool ok = true;
-        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+        for (int64_t i = 0; ok; ++i) {
+            int32_t idx = -1;
+            if (lane == 0) ok = queue_claim(p.sched, p.n_items, ring, bar.item_full, bar.item_empty, i, abort_flag,
+                                            p.wait_limit_ns, idx);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            if (!ok || idx < 0) break;
+            queue_decode(p, idx, it);
             if (it.nch == 0) continue;
-            // Warm L2 with the next non-empty item's Q tile while this one streams.
-            if (lane == 0) {
-                for (int64_t r2 = round + 1; item_at(p, r2, nx); ++r2)
-                    if (nx.nch > 0) {
-                        for (int kb = 0; kb < 4; ++kb)
-                            tma_prefetch_4d(&p.q_map, kb * 64, (int)(nx.g * p.G), (int)(nx.t * p.T), (int)nx.b);
-                        break;
-                    }
-            }
+            // Warm L2 with the item's Q tile; the softmax warps copy it into TMEM a little later.
+            if (lane == 0)
+                for (int kb = 0; kb < 4; ++kb)
+                    tma_prefetch_4d(&p.q_map, kb * 64, (int)(it.g * p.G), (int)(it.t * p.T), (int)it.b);
             const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
             const KVMaps &maps = p.kv[pair];
             const int32_t *keys = p.tile_keys + it.tile * p.max_chunks * kChunkKeys;
@@ -286,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             gc += it.nch;
         }
         if (!ok && lane == 0) fail(kSiteTileFwdWait, 1);
+        if (lane == 0) queue_finish(p.sched);
         // Drain: every issued copy must have landed before the CTA leaves.
         if (lane == 0) {
             bool drained = true;
@@ -340,7 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             int64_t gc = 0, qc = 0;
             Item it;
             bool ok = true;
-            for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+            for (int64_t i = 0; ok; ++i) {
+                int32_t idx = -1;
+                ok = queue_take(ring, bar.item_full, bar.item_empty, i, abort_flag, p.wait_limit_ns, false, idx);
+                if (!ok || idx < 0) break;
+                queue_decode(p, idx, it);
                 if (it.nch == 0) continue;
                 const int n = it.nch;
                 ok = wait1(bar.q_ready, qc);
@@ -377,7 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         Item it;
         bool ok = true;
         bool have_q = false;  // Q of the current item is already in TMEM
-        for (int64_t round = 0; ok && item_at(p, round, it); ++round) {
+        int64_t pos = 0;      // ring position of the current item
+        int32_t idx = -1;
+        ok = queue_take(ring, bar.item_full, bar.item_empty, 0, abort_flag, p.wait_limit_ns, true, idx);
+        while (ok && idx >= 0) {
+            queue_decode(p, idx, it);
             const int64_t q = it.t * p.T + qi;
             const int64_t h = it.g * p.G + hl;
             const bool live = q < p.S_q;
@@ -388,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     for (int i = 0; i < kHeadDim / 8; ++i) reinterpret_cast<uint4 *>(orow)[i] = z;
                     p.lse[(it.b * p.Hq + h) * p.S_q + q] = -INFINITY;
                 }
+                ok = queue_take(ring, bar.item_full, bar.item_empty, ++pos, abort_flag, p.wait_limit_ns, true, idx);
                 continue;
             }
             if (!have_q) {  // only for the first non-empty item; later ones are loaded ahead
@@ -463,24 +469,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 mbar_arrive(bar.p_full + st);
             }
             if (!ok) break;
-            // Load the next non-empty item's Q once this item's last S has read the current one, so the
-            // MMA warp can start it while this epilogue runs.
-            have_q = false;
-            Item nx;
-            for (int64_t r2 = round + 1; item_at(p, r2, nx); ++r2) {
-                if (nx.nch == 0) continue;
-                if (!wait(bar.q_free, qc)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                load_q_row(p, nx, qi, hl, trow);
-                tc_fence_before();
-                mbar_arrive(bar.q_ready);
-                have_q = true;
+            // Take the next item now and, if it has chunks, load its Q once this item's last S has read
+            // the current one, so the MMA thread can start it while this epilogue runs.
+            int32_t nidx = -1;
+            if (!queue_take(ring, bar.item_full, bar.item_empty, pos + 1, abort_flag, p.wait_limit_ns, true, nidx)) {
+                ok = false;
                 break;
             }
-            if (!ok) break;
+            have_q = false;
+            if (nidx >= 0) {
+                Item nx;
+                queue_decode(p, nidx, nx);
+                if (nx.nch > 0) {
+                    if (!wait(bar.q_free, qc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    load_q_row(p, nx, qi, hl, trow);
+                    tc_fence_before();
+                    mbar_arrive(bar.q_ready);
+                    have_q = true;
+                }
+            }
             // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)) once the item's last PV has landed.
             if (!wait(bar.o_ready + (gc - 1) % kStages, (gc - 1) / kStages)) {
                 ok = false;
@@ -507,6 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             mbar_arrive(bar.o_free);
             if (live) p.lse[(it.b * p.Hq + h) * p.S_q + q] = l > 0.f ? (m + __log2f(l)) * kLn2 : -INFINITY;
             ++qc;
+            ++pos;
+            idx = nidx;
         }
         if (!ok) fail(kSiteTileFwdWait, 4);
     }
@@ -555,6 +568,7 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
     p.tile_keys = t.tile_keys;
     p.tile_masks = t.tile_masks;
     p.order = t.order;
+    p.sched = t.sched;  // forward counters
     p.o = o;
     p.lse = lse;
     p.status = a.status;

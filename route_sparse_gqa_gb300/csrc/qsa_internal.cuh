@@ -28,7 +28,7 @@ struct Layout {
     int64_t T;           // queries per tile (kTileRows / G), 0 when the tile path does not apply
     int64_t n_tiles;     // query tiles per batch row
     int64_t max_chunks;  // capacity of one tile's chunk list
-    size_t off_status, off_counts, off_ids, off_tile_nchunks, off_tile_keys, off_tile_masks, off_order;
+    size_t off_status, off_sched, off_counts, off_ids, off_tile_nchunks, off_tile_keys, off_tile_masks, off_order;
     size_t off_delta, off_dk, off_dv, total;
 };
 

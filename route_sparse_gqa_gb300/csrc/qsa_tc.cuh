@@ -16,6 +16,7 @@ struct TileArgs {
     const int32_t *tile_keys;
     const uint64_t *tile_masks;
     const int32_t *order;
+    int32_t *sched;  // {next, done} work queue counters: [0..1] forward, [2..3] backward; zero between launches
 };
 
 // Host helpers shared by the tile kernels (qsa_tc_host.cu).
