@@ -230,28 +230,41 @@ def run_ours(args):
 
     peaks, peak_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops"])  # burst figure: each entry point runs well under a second
+    fwd_tf = wc["fwd_flop"] / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = wc["bwd_flop"] / (bwd_ms * 1e-3) / 1e12
     fwd_gbs = wc["fwd_bytes"] / (fwd_ms * 1e-3) / 1e9
     bwd_gbs = wc["bwd_bytes"] / (bwd_ms * 1e-3) / 1e9
     dominant = "backward" if bwd_ms >= fwd_ms else "forward"
-    kern = {"forward": ("qsa_forward", fwd_gbs, wc["fwd_bytes"], fwd_ms),
-            "backward": ("qsa_backward", bwd_gbs, wc["bwd_bytes"], bwd_ms)}[dominant]
+    kern = {"forward": ("qsa_forward", fwd_tf, wc["fwd_flop"], fwd_ms),
+            "backward": ("qsa_backward", bwd_tf, wc["bwd_flop"], bwd_ms)}[dominant]
+    # The tile kernels reuse every gathered K/V row for all 128 rows of a tile, so their DRAM traffic is far
+    # below the per-row gathered bytes; the binding peak is the tensor pipe.  Useful FLOP (valid routes only)
+    # never exceed executed FLOP, so achieved/peak is a true fraction.  The gathered-bytes view is kept below.
     roofline = {
-        "bound": "hbm",
-        "achieved": round(kern[1], 1),
-        "peak": hbm,
-        "unit": "GB/s",
-        "frac": round(kern[1] / hbm, 4),
+        "bound": "tensor",
+        "achieved": round(kern[1], 2),
+        "peak": tc_peak,
+        "unit": "TFLOP/s",
+        "frac": round(kern[1] / tc_peak, 4),
         "traffic": recorded_traffic(kern[0]),
         "kernel": kern[0],
-        "algorithmic_bytes_per_launch": kern[2],
+        "algorithmic_flop_per_launch": kern[2],
         "launch_ms": round(kern[3], 4),
-        "peak_source": f"{peak_src} MEASURED_PEAKS.json hbm_gbs" if peak_src == "measured" else "fallback",
-        "fwd_frac": round(fwd_gbs / hbm, 4),
-        "bwd_frac": round(bwd_gbs / hbm, 4),
-        "fwd_tflops": round(wc["fwd_flop"] / (fwd_ms * 1e-3) / 1e12, 2),
-        "bwd_tflops": round(wc["bwd_flop"] / (bwd_ms * 1e-3) / 1e12, 2),
-        "fwd_tensor_frac": round(wc["fwd_flop"] / (fwd_ms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4),
-        "bwd_tensor_frac": round(wc["bwd_flop"] / (bwd_ms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]), 4),
+        "peak_source": (f"{peak_src} MEASURED_PEAKS.json bf16_tflops" if peak_src == "measured"
+                        else "fallback 1.9 PFLOP/s"),
+        "fwd_tflops": round(fwd_tf, 2),
+        "bwd_tflops": round(bwd_tf, 2),
+        "fwd_frac": round(fwd_tf / tc_peak, 4),
+        "bwd_frac": round(bwd_tf / tc_peak, 4),
+        "gathered_bytes": {
+            "note": "per-row K/V gather model (no reuse); DRAM traffic is far lower, so fractions exceed 1",
+            "fwd_gbs": round(fwd_gbs, 1),
+            "bwd_gbs": round(bwd_gbs, 1),
+            "fwd_frac_of_hbm": round(fwd_gbs / hbm, 3),
+            "bwd_frac_of_hbm": round(bwd_gbs / hbm, 3),
+            "hbm_peak_gbs": hbm,
+        },
     }
     cpu = run_cpu_baseline(case, w, args) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     line = {
