@@ -84,9 +84,11 @@ struct BwdParams {
 
 using Item = QueueItem;
 
+// kSFull: S of the chunk complete; kSDFull: dP complete too (S is issued first so the softmax can
+// start on P while dP runs).
 enum BarId {
     kQFull, kQEmpty, kKFull, kKEmpty, kVFull, kVEmpty, kSDFull, kPDSFull, kPDSEmpty, kGradsFull, kFlushDone,
-    kDQReady, kDQFree, kDrain
+    kDQReady, kDQFree, kDrain, kSFull
 };
 
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
@@ -100,8 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     const uint32_t sbase = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[kDrain + 1] = {1, 1, 1, 1, 1, 1, 1, 128, 1, 1, 128, 1, 128, 1};
-        for (int i = 0; i <= kDrain; ++i) mbar_init(bars + i, counts[i]);
+        const uint32_t counts[kSFull + 1] = {1, 1, 1, 1, 1, 1, 1, 128, 1, 1, 128, 1, 128, 1, 1};
+        for (int i = 0; i <= kSFull; ++i) mbar_init(bars + i, counts[i]);
         for (int i = 0; i < kQueueRing; ++i) {
             mbar_init(bars + kBarItemFull + i, 1);
             mbar_init(bars + kBarItemEmpty + i, 32 + 128 + 128);  // MMA warp, softmax and flush threads take every item
@@ -240,18 +242,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 if (lane == 0) {
+                    // S first (its own completion barrier), then dP.
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t off = kb * (kTileBytes / 4) + k * 32;
-                            const uint32_t koff = kb * (kKVBytes / 4) + k * 32;
-                            const uint32_t acc = (kb | k) ? 1u : 0u;
-                            mma_bf16(tmem + kTmemS, sdesc_sw128(sbase + kOffQ + off, 16, 1024),
-                                     sdesc_sw128(sbase + kOffK + koff, 16, 1024), idesc_n64, acc);
-                            mma_bf16(tmem + kTmemDP, sdesc_sw128(sbase + kOffDO + off, 16, 1024),
-                                     sdesc_sw128(sbase + kOffV + koff, 16, 1024), idesc_n64, acc);
-                        }
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16(tmem + kTmemS, sdesc_sw128(sbase + kOffQ + kb * (kTileBytes / 4) + k * 32, 16, 1024),
+                                     sdesc_sw128(sbase + kOffK + kb * (kKVBytes / 4) + k * 32, 16, 1024), idesc_n64,
+                                     (kb | k) ? 1u : 0u);
+                    }
+                    mma_commit(bars + kSFull);
+#pragma unroll
+                    for (int kb = 0; kb < 4; ++kb) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16(tmem + kTmemDP, sdesc_sw128(sbase + kOffDO + kb * (kTileBytes / 4) + k * 32, 16, 1024),
+                                     sdesc_sw128(sbase + kOffV + kb * (kKVBytes / 4) + k * 32, 16, 1024), idesc_n64,
+                                     (kb | k) ? 1u : 0u);
                     }
                     mma_commit(bars + kSDFull);
                     mma_commit(bars + kVEmpty);
@@ -338,36 +345,43 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 const uint64_t mask = mask_next;
                 if (c + 1 < it.nch) mask_next = __ldg(mrow + (c + 1) * p.T);
+                if (!wait(kSFull, gc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float pf[64];
+                {
+                    uint32_t sr[2][32];
+                    tmem_ld32(trow + kTmemS, sr[0]);
+                    tmem_ld32(trow + kTmemS + 32, sr[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        pf[j] = ((mask >> j) & 1ull) ? ex2(__uint_as_float(sr[j >> 5][j & 31]) * p.sl2 - lse2) : 0.f;
+                }
                 if (!wait(kSDFull, gc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t sr[2][32], dr[2][32];
-                tmem_ld32(trow + kTmemS, sr[0]);
-                tmem_ld32(trow + kTmemS + 32, sr[1]);
-                tmem_ld32(trow + kTmemDP, dr[0]);
-                tmem_ld32(trow + kTmemDP + 32, dr[1]);
-                tmem_ld_wait();
+                uint32_t pk[32], dk[32];
+                {
+                    uint32_t dr[2][32];
+                    tmem_ld32(trow + kTmemDP, dr[0]);
+                    tmem_ld32(trow + kTmemDP + 32, dr[1]);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 64; j += 2) {
+                        const float d0 = p.scale * pf[j] * (__uint_as_float(dr[j >> 5][j & 31]) - delta);
+                        const float d1 = p.scale * pf[j + 1] * (__uint_as_float(dr[(j + 1) >> 5][(j + 1) & 31]) - delta);
+                        pk[j >> 1] = pack_bf16(pf[j], pf[j + 1]);
+                        dk[j >> 1] = pack_bf16(d0, d1);
+                    }
+                }
                 if (gc > 0 && !wait(kPDSEmpty, gc - 1)) {
                     ok = false;
                     break;
-                }
-                uint32_t pk[32], dk[32];
-#pragma unroll
-                for (int j = 0; j < 64; j += 2) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int jj = j + e;
-                        const bool in = (mask >> jj) & 1ull;
-                        const float s = __uint_as_float(sr[jj >> 5][jj & 31]);
-                        const float dp = __uint_as_float(dr[jj >> 5][jj & 31]);
-                        pv[e] = in ? ex2(s * p.sl2 - lse2) : 0.f;
-                        dv[e] = p.scale * pv[e] * (dp - delta);
-                    }
-                    pk[j >> 1] = pack_bf16(pv[0], pv[1]);
-                    dk[j >> 1] = pack_bf16(dv[0], dv[1]);
                 }
                 uint8_t *prow = smem + kOffP + r * 128;
                 uint8_t *drow = smem + kOffDS + r * 128;
