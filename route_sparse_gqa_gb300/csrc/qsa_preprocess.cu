@@ -33,6 +33,7 @@ constexpr int kTileThreads = 256;
 constexpr int kTileWindow = 4096;  // keys per window of the shared-memory membership table
 constexpr int kRowWindowBits = 65536;  // keys per window of a row's shared-memory bitmap (8 KiB)
 constexpr int kRowMaxWindows = 8;      // wider rows fall back to the bitonic sort
+constexpr int kRowCache = 8;           // route slots per thread kept in registers (K <= 8 * kRowThreads)
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -81,13 +82,30 @@ __global__ void __launch_bounds__(kRowThreads) route_rows_kernel(RowsArgs a, int
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     int32_t *out = a.ids + row * a.K;
 
-    // Range of the valid ids (validity tested in the route's own width).
+    // Range of the valid ids (validity tested in the route's own width).  Rows of up to
+    // kRowCache * blockDim.x slots are read once and kept in registers for the bitmap pass.
+    const bool cached = a.K <= (int64_t)kRowCache * blockDim.x;
+    int32_t cache[kRowCache];
     int64_t lo = INT64_MAX, hi = -1;
-    for (int64_t i = tid; i < a.K; i += blockDim.x) {
-        const int64_t x = load_route(a, b, q, i);
-        if (x >= 0 && x < a.S_kv) {
-            lo = min(lo, x);
-            hi = max(hi, x);
+    if (cached) {
+#pragma unroll
+        for (int j = 0; j < kRowCache; ++j) {
+            const int64_t i = tid + (int64_t)j * blockDim.x;
+            const int64_t x = i < a.K ? load_route(a, b, q, i) : -1;
+            const bool valid = x >= 0 && x < a.S_kv;
+            cache[j] = valid ? (int32_t)x : -1;
+            if (valid) {
+                lo = min(lo, x);
+                hi = max(hi, x);
+            }
+        }
+    } else {
+        for (int64_t i = tid; i < a.K; i += blockDim.x) {
+            const int64_t x = load_route(a, b, q, i);
+            if (x >= 0 && x < a.S_kv) {
+                lo = min(lo, x);
+                hi = max(hi, x);
+            }
         }
     }
 #pragma unroll
@@ -113,9 +131,17 @@ __global__ void __launch_bounds__(kRowThreads) route_rows_kernel(RowsArgs a, int
             const int nwords = (int)((span + 31) / 32);
             for (int i = tid; i < nwords; i += blockDim.x) rsm[i] = 0u;
             __syncthreads();
-            for (int64_t i = tid; i < a.K; i += blockDim.x) {
-                const int64_t x = load_route(a, b, q, i);
-                if (x >= w0 && x < w0 + span) atomicOr(&rsm[(x - w0) >> 5], 1u << ((x - w0) & 31));
+            if (cached) {
+#pragma unroll
+                for (int j = 0; j < kRowCache; ++j) {
+                    const int64_t x = cache[j];  // -1 for invalid or missing slots
+                    if (x >= w0 && x < w0 + span) atomicOr(&rsm[(x - w0) >> 5], 1u << ((x - w0) & 31));
+                }
+            } else {
+                for (int64_t i = tid; i < a.K; i += blockDim.x) {
+                    const int64_t x = load_route(a, b, q, i);
+                    if (x >= w0 && x < w0 + span) atomicOr(&rsm[(x - w0) >> 5], 1u << ((x - w0) & 31));
+                }
             }
             __syncthreads();
             const int per = (nwords + blockDim.x - 1) / blockDim.x;
