@@ -29,8 +29,9 @@ namespace qsa {
 namespace {
 
 constexpr int kRowThreads = 256;
-constexpr int kTileThreads = 256;
+constexpr int kTileThreads = 512;
 constexpr int kTileWindow = 4096;  // keys per window of the shared-memory membership table
+constexpr int kTileBatches = 8;   // 32-id batches of one row read per step (independent loads)
 constexpr int kRowWindowBits = 65536;  // keys per window of a row's shared-memory bitmap (8 KiB)
 constexpr int kRowMaxWindows = 8;      // wider rows fall back to the bitonic sort
 constexpr int kRowCache = 8;           // route slots per thread kept in registers (K <= 8 * kRowThreads)
@@ -253,14 +254,30 @@ __global__ void __launch_bounds__(kTileThreads) route_tiles_kernel(TilesArgs a) 
             const int32_t *row = a.ids + (b * a.S_q + q0 + qi) * a.K;
             int p = ptr[qi];
             const int c = cnt[qi];
-            while (p < c) {
-                const int idx = p + lane;
-                const int64_t id = idx < c ? (int64_t)row[idx] : INT64_MAX;
-                const bool in = id < w0 + kTileWindow;
-                if (in) atomicOr(&mem[id - w0], 1u << qi);
-                const int n_in = __popc(__ballot_sync(0xffffffffu, in));
-                p += n_in;
-                if (n_in < 32) break;
+            // kTileBatches batches of 32 ids per step, loaded independently; ids ascend, so the
+            // window ends in the first batch that is not entirely inside it.
+            bool more = p < c;
+            while (more) {
+                int64_t id[kTileBatches];
+#pragma unroll
+                for (int u = 0; u < kTileBatches; ++u) {
+                    const int idx = p + u * 32 + lane;
+                    id[u] = idx < c ? (int64_t)row[idx] : INT64_MAX;
+                }
+                int n_step = 0;
+#pragma unroll
+                for (int u = 0; u < kTileBatches; ++u) {
+                    const bool in = id[u] < w0 + kTileWindow;
+                    if (in) atomicOr(&mem[id[u] - w0], 1u << qi);
+                    const int n_in = __popc(__ballot_sync(0xffffffffu, in));
+                    n_step += n_in;
+                    if (n_in < 32) {
+                        more = false;
+                        break;
+                    }
+                }
+                p += n_step;
+                more = more && p < c;
             }
             if (lane == 0) ptr[qi] = p;
         }
