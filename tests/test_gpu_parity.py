@@ -189,3 +189,43 @@ def test_route_sets_wide_and_narrow_ranges():
     ids_ref, counts_ref = oracle.route_sets(routes, S_kv)
     assert np.array_equal(counts.cpu().numpy(), counts_ref)
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
+
+
+def test_repeated_calls_share_one_workspace():
+    """The tile kernels take their work from a queue whose counters live in the
+    workspace and are reset by the last CTA of every launch.  Calls repeated on
+    one plan must therefore give the same results: O, LSE and dQ bit for bit (each
+    item is computed by one CTA in a fixed order), dK and dV within the tolerance
+    (fp32 reductions in any order), all matching the oracle; a tile count below
+    the SM count and one far above it are both exercised."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+    from tests.qsa_testlib import bf16_to_device
+
+    dev = torch.device("cuda:0")
+    for seed, (B, S_q, S_kv, Hq, Hkv, K) in ((41, (1, 40, 96, 16, 2, 24)), (42, (2, 1200, 700, 16, 2, 40))):
+        q, k, v, do, routes = _random_case(seed, B, S_q, S_kv, Hq, Hkv, K)
+        qt, kt, vt, dot = (bf16_to_device(x, dev) for x in (q, k, v, do))
+        rt = torch.from_numpy(routes).to(dev)
+        plan = qsa.preprocess(qt, kt, vt, rt, 1.0 / 16)
+        outs = []
+        for _ in range(3):
+            o, lse = qsa.forward(plan, qt, kt, vt)
+            dq, dk, dv = qsa.backward(plan, qt, kt, vt, o, lse, dot)
+            outs.append([x.float().cpu().numpy() for x in (o, lse, dq, dk, dv)])
+        plan.device_status()
+        for later in outs[1:]:
+            for name, a, b in zip(("O", "LSE", "dQ"), outs[0][:3], later[:3]):
+                assert np.array_equal(a, b, equal_nan=True), f"{name} differs between repeated calls"
+            for name, a, b in zip(("dK", "dV"), outs[0][3:], later[3:]):
+                assert_close(name + " repeat", b.astype(np.float64), a.astype(np.float64))
+        qd, kd, vd, dod = f64(q), f64(k), f64(v), f64(do)
+        o_ref, lse_ref = oracle.forward(qd, kd, vd, routes, 1.0 / 16)
+        dq_ref, dk_ref, dv_ref = oracle.backward(qd, kd, vd, routes, dod, 1.0 / 16)
+        last = outs[-1]
+        assert_close("O", last[0].astype(np.float64), o_ref)
+        assert_lse_close(last[1].astype(np.float64), lse_ref)
+        assert_close("dQ", last[2].astype(np.float64), dq_ref)
+        assert_close("dK", last[3].astype(np.float64), dk_ref)
+        assert_close("dV", last[4].astype(np.float64), dv_ref)
