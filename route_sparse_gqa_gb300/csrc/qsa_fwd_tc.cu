@@ -99,6 +99,11 @@ struct FwdParams {
 
 using Item = QueueItem;
 
+// Stage (ring slot, barrier index) and barrier phase parity of global chunk g.  Chunk numbers of one
+// CTA stay far below 2^31, so 32-bit arithmetic (a multiply-high for the division) suffices.
+__device__ __forceinline__ int stage_of(int64_t g) { return (int)((uint32_t)g % (uint32_t)kStages); }
+__device__ __forceinline__ int64_t round_of(int64_t g) { return (int64_t)((uint32_t)g / (uint32_t)kStages); }
+
 // Per-chunk barriers are indexed by the global chunk number c modulo kStages
 // (the K/V stage of chunk c); the S/P TMEM buffer of chunk c is c % 2.
 struct Bars {
@@ -243,13 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 bool run = false;
                 if (c < it.nch) {
                     const int64_t gk = gc + c;
-                    const int sk = (int)(gk % kStages);
+                    const int sk = stage_of(gk);
                     if (lane < 16) kk = __ldg(reinterpret_cast<const int4 *>(keys + c * kChunkKeys) + lane);
                     first = __shfl_sync(0xffffffffu, kk.x, 0);
                     const int last = __shfl_sync(0xffffffffu, kk.w, 15);
                     run = last - first == kChunkKeys - 1;  // ascending distinct keys: a contiguous run
                     // The stage is free once S of chunk gk - kStages (which read it) has completed.
-                    if (gk >= kStages && !wait(bar.s_full + sk, gk / kStages - 1)) {
+                    if (gk >= kStages && !wait(bar.s_full + sk, round_of(gk) - 1)) {
                         ok = false;
                         break;
                     }
@@ -262,9 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 if (c > 0) {
                     const int64_t gv = gc + c - 1;
-                    const int sv = (int)(gv % kStages);
+                    const int sv = stage_of(gv);
                     // ... and once PV of chunk gv - kStages has completed.
-                    if (gv >= kStages && !wait(bar.o_ready + sv, gv / kStages - 1)) {
+                    if (gv >= kStages && !wait(bar.o_ready + sv, round_of(gv) - 1)) {
                         ok = false;
                         break;
                     }
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 return mbar_wait(b, (uint32_t)(phase & 1), abort_flag, p.wait_limit_ns);
             };
             auto issue_s = [&](int64_t g2, bool last_s) {
-                const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
+                const int s = stage_of(g2), sb = (int)(g2 & 1);
                 const uint32_t ka = sbase + kOffK + s * kKVBytes;
                 const uint32_t sp = tmem + kTmemSP + sb * kChunkKeys;
 #pragma unroll
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 if (last_s) mma_commit(bar.q_free);  // the item's Q in TMEM is no longer read
             };
             auto issue_pv = [&](int64_t g2, bool first) {
-                const int s = (int)(g2 % kStages), sb = (int)(g2 & 1);
+                const int s = stage_of(g2), sb = (int)(g2 & 1);
                 const uint32_t va = sbase + kOffV + s * kKVBytes;
                 const uint32_t pa = tmem + kTmemSP + sb * kChunkKeys;
 #pragma unroll
@@ -346,15 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 const int n = it.nch;
                 ok = wait1(bar.q_ready, qc);
                 for (int c = 0; ok && c < n && c < 2; ++c) {
-                    ok = wait1(bar.k_full + (gc + c) % kStages, (gc + c) / kStages);
+                    ok = wait1(bar.k_full + stage_of(gc + c), round_of(gc + c));
                     tc_fence_after();
                     if (ok) issue_s(gc + c, c == n - 1);
                 }
                 for (int c = 0; ok && c < n; ++c) {
                     const int64_t g2 = gc + c;
-                    ok = wait1(bar.p_full + g2 % kStages, g2 / kStages) && wait1(bar.v_full + g2 % kStages, g2 / kStages) &&
-                         (c > 0 || qc == 0 || wait1(bar.o_free, qc - 1)) &&
-                         (c + 2 >= n || wait1(bar.k_full + (g2 + 2) % kStages, (g2 + 2) / kStages));
+                    // One wait per pair: the softmax warps arrive on p_full(c) only after they have also seen
+                    // V(c) and, within the item, K(c+2) land, so this barrier covers every operand of PV(c) and
+                    // S(c+2).  (Each barrier wait costs this thread a few hundred cycles once it has MMAs queued.)
+                    ok = wait1(bar.p_full + stage_of(g2), round_of(g2)) && (c > 0 || qc == 0 || wait1(bar.o_free, qc - 1));
                     tc_fence_after();
                     if (!ok) break;
                     issue_pv(g2, c == 0);
@@ -405,11 +411,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             uint64_t mask_next = __ldg(mrow);
             float m = -INFINITY, l = 0.f;
             for (int c = 0; c < it.nch; ++c, ++gc) {
-                const int sb = (int)(gc & 1), st = (int)(gc % kStages);
+                const int sb = (int)(gc & 1), st = stage_of(gc);
                 const uint32_t sp = trow + kTmemSP + sb * kChunkKeys;
                 const uint64_t mask = mask_next;
                 if (c + 1 < it.nch) mask_next = __ldg(mrow + (c + 1) * p.T);
-                if (!wait(bar.s_full + st, gc / kStages)) {
+                // V(c) and, within the item, K(c+2) must have landed before P(c) is released: the MMA thread
+                // waits only for P(c) before issuing PV(c) and S(c+2).  V(c) is in shared memory long before
+                // S(c) completes (waited here); K(c+2) can only be loaded once S(c-1) has freed its stage, so
+                // it is waited for after the softmax math, just before P(c) is released.  Parity safety: the
+                // producer reuses a stage only after the S (K) or PV (V) three chunks back completed, and
+                // those need P of chunks this thread has not released yet, so neither barrier can be a
+                // phase ahead; and the phase before (three chunks back) completed before S(c-1) did.
+                if (!wait(bar.v_full + st, round_of(gc))) {
+                    ok = false;
+                    break;
+                }
+                if (!wait(bar.s_full + st, round_of(gc))) {
                     ok = false;
                     break;
                 }
@@ -432,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     // complete, so every MMA issued before it is too, among them the PV three chunks
                     // back that completed the previous phase of this barrier: the parity wait below
                     // can only mean PV(c-1), and PV(c+2) cannot complete before P(c+2) exists.
-                    if (!wait(bar.o_ready + (gc - 1) % kStages, (gc - 1) / kStages)) {
+                    if (!wait(bar.o_ready + stage_of(gc - 1), round_of(gc - 1))) {
                         ok = false;
                         break;
                     }
@@ -465,6 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 l += lsum;
                 tmem_st32(sp, pk);  // P over the first half of the S buffer it came from
                 tmem_st_wait();
+                if (c + 2 < it.nch && !wait(bar.k_full + stage_of(gc + 2), round_of(gc + 2))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_before();
                 mbar_arrive(bar.p_full + st);
             }
@@ -493,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
             }
             // Epilogue: O = acc / l (BF16), LSE = ln(sum exp(s)) once the item's last PV has landed.
-            if (!wait(bar.o_ready + (gc - 1) % kStages, (gc - 1) / kStages)) {
+            if (!wait(bar.o_ready + stage_of(gc - 1), round_of(gc - 1))) {
                 ok = false;
                 break;
             }

@@ -58,17 +58,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds (or at once when *abort is set by another role) and
 // returns false; the caller then records a timeout and winds down.  A limit of
-// 0 (test hook) only tests the phase once, without blocking.
+// 0 (test hook) only tests the phase once, without blocking.  The clock (a slow
+// read) is first read after 64 unsuccessful polls, so the common short waits
+// never touch it; the bound then runs from that first read.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort,
                                           uint64_t limit_ns) {
     if (limit_ns == 0) return mbar_test_wait(bar, parity);
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > limit_ns) return false;
         }
     }
 }
