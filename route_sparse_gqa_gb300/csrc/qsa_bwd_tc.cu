@@ -173,15 +173,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     ok = false;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bars + kVFull, kKVBytes);
+                // One barrier covers the chunk's K and V (the MMA warp waits once): the arrival announces
+                // both copies' bytes, V's copy goes out now and K's once its slot is free.
+                if (lane == 0) mbar_arrive_expect_tx(bars + kKFull, 2 * kKVBytes);
                 __syncwarp();
                 if (run) {
                     if (lane == 0)
                         for (int kb = 0; kb < 4; ++kb)
-                            tma_load_2d(sbase + kOffV + kb * (kKVBytes / 4), &maps.v_run, bars + kVFull, kb * 64, first);
+                            tma_load_2d(sbase + kOffV + kb * (kKVBytes / 4), &maps.v_run, bars + kKFull, kb * 64, first);
                 } else if (lane < 16) {
                     for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(sbase + kOffV + lane * 512 + kb * (kKVBytes / 4), &maps.v_rows, bars + kVFull,
+                        tma_gather4(sbase + kOffV + lane * 512 + kb * (kKVBytes / 4), &maps.v_rows, bars + kKFull,
                                     kb * 64, kk.x, kk.y, kk.z, kk.w);
                 }
                 __syncwarp();
@@ -190,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     ok = false;
                     break;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bars + kKFull, kKVBytes);
                 __syncwarp();
                 if (run) {
                     if (lane == 0)
@@ -210,8 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // Drain every issued copy before the CTA can leave.
         if (lane == 0) {
             bool drained = true;
-            if (v_issued > 0) drained &= mbar_wait(bars + kVFull, (uint32_t)((v_issued - 1) & 1), &zero, kWaitLimitNs);
-            if (k_issued > 0) drained &= mbar_wait(bars + kKFull, (uint32_t)((k_issued - 1) & 1), &zero, kWaitLimitNs);
+            // The last chunk's K and V phase; if the producer gave up between the V and the K copy, this
+            // wait runs to its bound (the V copy has long landed by then).
+            if (v_issued > 0) drained &= mbar_wait(bars + kKFull, (uint32_t)((v_issued - 1) & 1), &zero, kWaitLimitNs);
+            (void)k_issued;
             if (qc > 0) drained &= mbar_wait(bars + kQFull, (uint32_t)((qc - 1) & 1), &zero, kWaitLimitNs);
             if (!drained) fail(2);
         }
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             }
             tc_fence_after();
             for (int c = 0; c < it.nch; ++c, ++gc) {
-                if (!wait(kKFull, gc) || !wait(kVFull, gc)) {
+                if (!wait(kKFull, gc)) {  // K and V of the chunk
                     ok = false;
                     break;
                 }
@@ -360,6 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     for (int j = 0; j < 64; ++j)
                         pf[j] = ((mask >> j) & 1ull) ? ex2(__uint_as_float(sr[j >> 5][j & 31]) * p.sl2 - lse2) : 0.f;
                 }
+                // The previous chunk's gradient MMAs have read the P/dS buffers (long done by now; waited
+                // here, off the path from dP to dS).
+                if (gc > 0 && !wait(kPDSEmpty, gc - 1)) {
+                    ok = false;
+                    break;
+                }
                 if (!wait(kSDFull, gc)) {
                     ok = false;
                     break;
@@ -378,10 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                         pk[j >> 1] = pack_bf16(pf[j], pf[j + 1]);
                         dk[j >> 1] = pack_bf16(d0, d1);
                     }
-                }
-                if (gc > 0 && !wait(kPDSEmpty, gc - 1)) {
-                    ok = false;
-                    break;
                 }
                 uint8_t *prow = smem + kOffP + r * 128;
                 uint8_t *drow = smem + kOffDS + r * 128;
