@@ -363,40 +363,43 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     for (int j = 0; j < 64; ++j)
                         pf[j] = ((mask >> j) & 1ull) ? ex2(__uint_as_float(sr[j >> 5][j & 31]) * p.sl2 - lse2) : 0.f;
                 }
-                // The previous chunk's gradient MMAs have read the P/dS buffers (long done by now; waited
-                // here, off the path from dP to dS).
+                // The previous chunk's gradient MMAs have read the P/dS buffers (long done by now); P goes
+                // into shared memory while the dP MMA still runs, so only dS is left once dP lands.
                 if (gc > 0 && !wait(kPDSEmpty, gc - 1)) {
                     ok = false;
                     break;
+                }
+                uint8_t *prow = smem + kOffP + r * 128;
+                uint8_t *drow = smem + kOffDS + r * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) w4[e] = pack_bf16(pf[8 * ch + 2 * e], pf[8 * ch + 2 * e + 1]);
+                    *reinterpret_cast<uint4 *>(prow + (ch ^ (r & 7)) * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
                 if (!wait(kSDFull, gc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                uint32_t pk[32], dk[32];
                 {
                     uint32_t dr[2][32];
                     tmem_ld32(trow + kTmemDP, dr[0]);
                     tmem_ld32(trow + kTmemDP + 32, dr[1]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 64; j += 2) {
-                        const float d0 = p.scale * pf[j] * (__uint_as_float(dr[j >> 5][j & 31]) - delta);
-                        const float d1 = p.scale * pf[j + 1] * (__uint_as_float(dr[(j + 1) >> 5][(j + 1) & 31]) - delta);
-                        pk[j >> 1] = pack_bf16(pf[j], pf[j + 1]);
-                        dk[j >> 1] = pack_bf16(d0, d1);
-                    }
-                }
-                uint8_t *prow = smem + kOffP + r * 128;
-                uint8_t *drow = smem + kOffDS + r * 128;
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t w4[4];
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const int phys = (ch ^ (r & 7)) * 16;
-                    *reinterpret_cast<uint4 *>(prow + phys) = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
-                                                                         pk[4 * ch + 3]);
-                    *reinterpret_cast<uint4 *>(drow + phys) = make_uint4(dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2],
-                                                                         dk[4 * ch + 3]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 8 * ch + 2 * e;
+                            const float d0 = p.scale * pf[j] * (__uint_as_float(dr[j >> 5][j & 31]) - delta);
+                            const float d1 = p.scale * pf[j + 1] * (__uint_as_float(dr[(j + 1) >> 5][(j + 1) & 31]) - delta);
+                            w4[e] = pack_bf16(d0, d1);
+                        }
+                        *reinterpret_cast<uint4 *>(drow + (ch ^ (r & 7)) * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
