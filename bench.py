@@ -331,10 +331,11 @@ def run_e2e(case, w, dev, args, qsa, flop_step, world):
     # results out inside the timed region; events order each buffer's reuse.
     comp = torch.cuda.current_stream(dev)
     h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    dev_in = [{name: torch.empty_like(t, device=dev) for name, t in host.items()} for _ in range(2)]
-    copied = [torch.cuda.Event() for _ in range(2)]   # inputs of a slot are on the device
-    used = [torch.cuda.Event() for _ in range(2)]     # compute finished with a slot's inputs
-    drained = [None, None]                            # results of a slot's last step are on the host
+    n_slots = int(os.environ.get("QSA_E2E_SLOTS", "2"))
+    dev_in = [{name: torch.empty_like(t, device=dev) for name, t in host.items()} for _ in range(n_slots)]
+    copied = [torch.cuda.Event() for _ in range(n_slots)]   # inputs of a slot are on the device
+    used = [torch.cuda.Event() for _ in range(n_slots)]     # compute finished with a slot's inputs
+    drained = [None] * n_slots                              # results of a slot's last step are on the host
 
     def copy_in(slot):
         with torch.cuda.stream(h2d_s):
@@ -361,11 +362,12 @@ def run_e2e(case, w, dev, args, qsa, flop_step, world):
         drained[slot] = done
 
     def run(n):
-        copy_in(0)
+        for i in range(min(n_slots - 1, n)):
+            copy_in(i % n_slots)
         for i in range(n):
-            if i + 1 < n:
-                copy_in((i + 1) % 2)
-            compute(i % 2)
+            if i + n_slots - 1 < n:
+                copy_in((i + n_slots - 1) % n_slots)
+            compute(i % n_slots)
         for e in drained:
             if e is not None:
                 comp.wait_event(e)
@@ -383,7 +385,7 @@ def run_e2e(case, w, dev, args, qsa, flop_step, world):
     ms = t0.elapsed_time(t1) / n
     return {"value": round(flop_step / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "pipeline": "inputs double-buffered on the device; step i+1's H2D and step i's D2H overlap step i's compute"}
+            "pipeline": f"inputs in {n_slots} device buffers; later steps' H2D and earlier steps' D2H overlap each step's compute"}
 
 
 def oracle_sample(case, w, rows_per_sample: int, seed: int = 0):
