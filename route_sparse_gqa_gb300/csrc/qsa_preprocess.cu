@@ -28,13 +28,13 @@
 namespace qsa {
 namespace {
 
-constexpr int kRowThreads = 256;
+constexpr int kRowThreads = 128;
 constexpr int kTileThreads = 512;
 constexpr int kTileWindow = 4096;  // keys per window of the shared-memory membership table
 constexpr int kTileBatches = 8;   // 32-id batches of one row read per step (independent loads)
 constexpr int kRowWindowBits = 65536;  // keys per window of a row's shared-memory bitmap (8 KiB)
 constexpr int kRowMaxWindows = 8;      // wider rows fall back to the bitonic sort
-constexpr int kRowCache = 8;           // route slots per thread kept in registers (K <= 8 * kRowThreads)
+constexpr int kRowCache = 16;          // route slots per thread kept in registers (K <= 16 * kRowThreads)
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
