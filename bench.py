@@ -152,6 +152,25 @@ def recorded_traffic(kernel: str):
     return entry.get("bytes_per_launch")
 
 
+def max_over_ranks(local_ms: float, device=None) -> float:
+    """The slowest replica's per-step time: every rank's own time reduced with MAX
+    (the local time when torch.distributed is not initialised)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(local_ms)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_step_per_rank: float, world: int, step_ms: float) -> float:
+    """Whole-job rate: every rank runs its own replica of the step (weak scaling),
+    so the job does world x the per-rank work in the slowest rank's time."""
+    return flop_per_step_per_rank * world / (step_ms * 1e-3) / 1e12
+
+
 def make_device_inputs(case, device):
     import torch
 
@@ -215,15 +234,12 @@ def run_ours(args):
         dist.barrier()
     per = np.array([[events[i][j].elapsed_time(events[i][j + 1]) for j in range(3)] for i in range(args.steps)])
     step_ms = float(per.sum(1).sum() / args.steps)
-    t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms_max = float(t.item())
+    step_ms_max = max_over_ranks(step_ms, dev)
     pre_ms, fwd_ms, bwd_ms = (float(x) for x in per.mean(0))
     plan.device_status()
 
     flop_step = wc["fwd_flop"] + wc["bwd_flop"]
-    value = flop_step * world / (step_ms_max * 1e-3) / 1e12
+    value = job_tflops(flop_step, world, step_ms_max)
 
     # End to end through the public API with pinned host buffers.
     e2e = run_e2e(case, w, dev, args, qsa, flop_step, world)
@@ -382,8 +398,8 @@ def run_e2e(case, w, dev, args, qsa, flop_step, world):
     run(n)
     t1.record(comp)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / n
-    return {"value": round(flop_step / (ms * 1e-3) / 1e12, 3), "unit": UNIT, "ms_per_step": round(ms, 4),
+    ms = max_over_ranks(t0.elapsed_time(t1) / n, dev)
+    return {"value": round(job_tflops(flop_step, world, ms), 3), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "pipeline": f"inputs in {n_slots} device buffers; later steps' H2D and earlier steps' D2H overlap each step's compute"}
 
