@@ -1,4 +1,4 @@
-"""ctypes view of libqsa's C ABI (include/qsa.h).  Marshalling only: every step
+"""ctypes view of libqsa's C ABI (include/qsa.h, include/qsa_route.h).  Marshalling only: every step
 of the attention runs in the library's CUDA kernels; nothing here computes."""
 from __future__ import annotations
 
@@ -20,7 +20,8 @@ STATUS_NAMES = {
     6: "QSA_ERR_DEVICE_CHECK",
 }
 
-# Every symbol include/qsa.h declares (checked by the tests against the built library).
+# Every symbol include/qsa.h and include/qsa_route.h declare (checked by the tests
+# against the built library).
 EXPORTS = (
     "qsa_check_problem",
     "qsa_workspace_bytes",
@@ -32,6 +33,12 @@ EXPORTS = (
     "qsa_read_device_status",
     "qsa_status_string",
     "qsa_last_error",
+    "qsa_route_check_problem",
+    "qsa_route_width",
+    "qsa_route_workspace_bytes",
+    "qsa_index_scores",
+    "qsa_select_from_scores",
+    "qsa_select_token_ids",
 )
 
 
@@ -49,6 +56,15 @@ class Problem(ctypes.Structure):
         ("route_bits", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
         ("q_stride", ctypes.c_int64 * 4), ("k_stride", ctypes.c_int64 * 4), ("v_stride", ctypes.c_int64 * 4),
         ("r_stride", ctypes.c_int64 * 3),
+    ]
+
+
+class RouteProblem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("S_q", ctypes.c_int64), ("H_index", ctypes.c_int64), ("D_index", ctypes.c_int64),
+        ("n_blocks", ctypes.c_int64), ("token_budget", ctypes.c_int64), ("compress_ratio", ctypes.c_int64),
+        ("query_position_offset", ctypes.c_int64),
+        ("q_stride", ctypes.c_int64 * 4), ("k_stride", ctypes.c_int64 * 3),
     ]
 
 
@@ -81,8 +97,18 @@ def load() -> ctypes.CDLL:
         lib.qsa_status_string.restype = ctypes.c_char_p
         lib.qsa_last_error.argtypes = []
         lib.qsa_last_error.restype = ctypes.c_char_p
+        R = ctypes.POINTER(RouteProblem)
+        lib.qsa_route_check_problem.argtypes = [R]
+        lib.qsa_route_width.argtypes = [R]
+        lib.qsa_route_width.restype = ctypes.c_int64
+        lib.qsa_route_workspace_bytes.argtypes = [R]
+        lib.qsa_route_workspace_bytes.restype = sz
+        lib.qsa_index_scores.argtypes = [R, vp, vp, vp, vp, sz, vp, vp]
+        lib.qsa_select_from_scores.argtypes = [R, vp, vp, vp, sz, vp, vp]
+        lib.qsa_select_token_ids.argtypes = [R, vp, vp, vp, vp, sz, vp, vp]
         for name in ("qsa_check_problem", "qsa_preprocess", "qsa_forward", "qsa_backward", "qsa_copy_route_sets",
-                     "qsa_forward_no_alloc", "qsa_read_device_status"):
+                     "qsa_forward_no_alloc", "qsa_read_device_status", "qsa_route_check_problem",
+                     "qsa_index_scores", "qsa_select_from_scores", "qsa_select_token_ids"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

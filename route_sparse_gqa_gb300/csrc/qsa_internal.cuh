@@ -41,6 +41,7 @@ enum Site : unsigned int {
     kSiteTileFwdKey = 11,
     kSiteTileBwdWait = 20,
     kSiteTileBwdKey = 21,
+    kSiteRouteScoreWait = 30,
 };
 
 __device__ __forceinline__ void raise_status(DeviceStatus *st, unsigned int code, unsigned int where,

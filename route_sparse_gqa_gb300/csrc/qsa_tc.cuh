@@ -45,6 +45,12 @@ bool tc_encode_kv_maps(KVMaps *m, const AttnArgs &a, int64_t b, int64_t g);
 bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, int64_t B, int64_t sH, int64_t sS,
                         int64_t sB, int64_t G, int64_t T);
 
+// Generic BF16 tensor map, 128-byte swizzle, zero fill out of bounds: dims[0]
+// is the innermost (unit-stride) extent, strides[i] (elements) the pitch of
+// dimension i + 1, box the tile extents.
+bool tc_encode_bf16_map(CUtensorMap *m, const void *base, int rank, const int64_t *dims, const int64_t *strides,
+                        const uint32_t *box);
+
 bool tc_forward_supported();
 bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t);
 cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s);

@@ -87,4 +87,20 @@ bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, 
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tc_encode_bf16_map(CUtensorMap *m, const void *base, int rank, const int64_t *dims, const int64_t *strides,
+                        const uint32_t *box) {
+    if (rank < 2 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = (cuuint64_t)dims[i];
+        bx[i] = box[i];
+        estr[i] = 1;
+        if (i > 0) st[i - 1] = (cuuint64_t)strides[i - 1] * 2;
+    }
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base), d, st, bx, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace qsa

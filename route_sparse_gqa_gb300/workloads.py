@@ -35,6 +35,13 @@ Route recipes (each ID list is built in "generation order": the query's own
 Random numbers: ``numpy.random.Generator(PCG64(20261202 + index))``; routes are
 drawn first, then Q, K, V and dO, each ``standard_normal(float32)`` rounded to
 bfloat16 (round to nearest even).
+
+Route-producer inputs (``INDEX_WORKLOADS``, ``make_index_case``): index queries
+``[B,S_q,H,D]`` and compressed keys ``[B,NB,1,D]`` drawn from N(0, 1) and
+rounded to bfloat16 (the states the page's indexer feeds the selection are
+RMS-normalised and rotated, so unit-variance entries have their scale), plus
+right-padded logical lengths.  Generator ``PCG64(20261302 + index)``: queries
+first, then keys.
 """
 from __future__ import annotations
 
@@ -76,6 +83,54 @@ WORKLOADS = (
 )
 
 _ROWS_PER_PIECE = 2048
+
+
+@dataclasses.dataclass(frozen=True)
+class IndexWorkload:
+    index: int
+    name: str
+    B: int
+    S_q: int
+    S_global: int
+    offset: int  # global position of local query row 0
+    H: int
+    D: int
+    c: int
+    budget: int
+    lengths: tuple
+    summary: str
+
+    @property
+    def n_blocks(self) -> int:
+        return self.S_global // self.c
+
+
+INDEX_WORKLOADS = (
+    IndexWorkload(0, "index-small", 2, 1000, 1000, 0, 8, 128, 4, 64, (1000, 777),
+                  "B2 S1000 H8 D128 c4 budget64, seq 1 length 777"),
+    IndexWorkload(1, "index-right-padded", 2, 4096, 4096, 0, 32, 128, 4, 2048, (4096, 3000),
+                  "B2 S4096 H32 D128 c4 budget2048, seq 1 length 3000"),
+    IndexWorkload(2, "index-cp-shard", 1, 8192, 32768, 24576, 32, 128, 4, 2048, (32768,),
+                  "B1 local S_q8192 at global offset 24576 of S32768, H32 D128 c4 budget2048"),
+    IndexWorkload(3, "index-train-step", 1, 32768, 32768, 0, 32, 128, 4, 2048, (32768,),
+                  "B1 S32768 H32 D128 c4 budget2048 (8192 blocks, 512 chosen per row)"),
+)
+
+
+@dataclasses.dataclass
+class IndexCase:
+    workload: IndexWorkload
+    q: np.ndarray        # uint16 bf16 bits [B, S_q, H, D]
+    k: np.ndarray        # uint16 bf16 bits [B, NB, 1, D]
+    lengths: np.ndarray  # int64 [B]
+
+
+def make_index_case(index: int, seed: int | None = None) -> IndexCase:
+    w = INDEX_WORKLOADS[index]
+    rng = np.random.Generator(np.random.PCG64(SEED_BASE + 100 + index if seed is None else seed))
+    q = bf16_normal(rng, (w.B, w.S_q, w.H, w.D))
+    k = bf16_normal(rng, (w.B, w.n_blocks, 1, w.D))
+    return IndexCase(w, q, k, np.asarray(w.lengths, dtype=np.int64))
 
 
 def rng_for(index: int, seed: int | None = None) -> np.random.Generator:

@@ -1,7 +1,8 @@
-"""The C-ABI library builds, loads without a GPU, exports every symbol include/qsa.h
-declares, and rejects bad problems with the documented status codes before any
-device work (CPU only)."""
+"""The C-ABI library builds, loads without a GPU, exports every symbol
+include/qsa.h and include/qsa_route.h declare, and rejects bad problems with the
+documented status codes before any device work (CPU only)."""
 import ctypes
+import glob
 import math
 import os
 import re
@@ -11,7 +12,9 @@ import pytest
 
 from route_sparse_gqa_gb300 import _abi, build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qsa.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "qsa.h")
+HEADERS = sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +24,7 @@ def lib():
 
 
 def declared_symbols():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"QSA_API\s+[\w\s\*]*?\b(qsa_\w+)\s*\(", text)))
 
 
@@ -38,7 +41,8 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_header_compiles_as_c():
-    src = f'#include "{HEADER}"\nint main(void) {{ qsa_problem p; (void)p; return (int)QSA_OK; }}\n'
+    src = (f'#include "{HEADER}"\n#include "{os.path.join(INCLUDE, "qsa_route.h")}"\n'
+           'int main(void) { qsa_problem p; qsa_route_problem r; (void)p; (void)r; return (int)QSA_OK; }\n')
     r = subprocess.run(["gcc", "-x", "c", "-std=c99", "-fsyntax-only", "-I/usr/local/cuda/include", "-"],
                        input=src, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
@@ -121,3 +125,61 @@ def test_binding_fails_loudly_without_gpu_tensors(lib):
     r = torch.zeros(1, 4, 3, dtype=torch.int32)
     with pytest.raises(qsa.QSAError, match="CUDA tensor"):
         qsa.qsa_attention(q, k, k, r)
+
+
+def good_route_problem(**kw):
+    p = _abi.RouteProblem()
+    B, S_q, H, D, c = 2, 100, 32, 128, 4
+    p.B, p.S_q, p.H_index, p.D_index, p.n_blocks = B, S_q, H, D, S_q // c
+    p.token_budget, p.compress_ratio, p.query_position_offset = 64, c, 0
+    p.q_stride[0], p.q_stride[1], p.q_stride[2], p.q_stride[3] = S_q * H * D, H * D, D, 1
+    p.k_stride[0], p.k_stride[1], p.k_stride[2] = (S_q // c) * D, D, 1
+    for k, v in kw.items():
+        if k.endswith("_stride"):
+            arr = getattr(p, k)
+            for i, x in enumerate(v):
+                arr[i] = x
+        else:
+            setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, 0),
+    ({"H_index": 1}, 0),
+    ({"H_index": 128, "D_index": 64}, 0),
+    ({"token_budget": 0}, 0),
+    ({"n_blocks": 0, "S_q": 3}, 0),
+    ({"query_position_offset": 3}, 0),     # positions up to 102 < 25 * 4 + 3
+    ({"query_position_offset": 4}, 1),     # position 103 lies past the global sequence
+    ({"B": 0}, 1),
+    ({"compress_ratio": 0}, 1),
+    ({"token_budget": -1}, 1),
+    ({"query_position_offset": -1}, 1),
+    ({"H_index": 24}, 2),
+    ({"H_index": 256}, 2),
+    ({"D_index": 256}, 2),
+    ({"D_index": 96}, 2),
+    ({"n_blocks": 40000, "S_q": 160000}, 2),
+    ({"q_stride": (100 * 32 * 128, 32 * 128, 128, 2)}, 2),
+    ({"k_stride": (25 * 128, 132, 1)}, 2),
+])
+def test_route_problem_validation(lib, kw, status):
+    p = good_route_problem(**kw)
+    got = lib.qsa_route_check_problem(ctypes.byref(p))
+    assert got == status, lib.qsa_last_error()
+    n = lib.qsa_route_workspace_bytes(ctypes.byref(p))
+    assert (n > 0) == (status == 0)
+    w = lib.qsa_route_width(ctypes.byref(p))
+    assert w == (p.token_budget + p.compress_ratio - 1 if status == 0 else 0)
+    if status == 0:
+        assert n >= 512 + p.B * p.S_q * p.n_blocks * 4
+
+
+def test_route_host_side_errors_need_no_device(lib):
+    p = good_route_problem()
+    assert lib.qsa_select_token_ids(ctypes.byref(p), None, None, None, None, 0, None, None) == 1  # null tensors
+    one = ctypes.c_void_p(1 << 20)
+    assert lib.qsa_select_token_ids(ctypes.byref(p), one, one, one, ctypes.c_void_p(256), 0, one, None) == 3
+    assert lib.qsa_index_scores(ctypes.byref(p), one, one, one, ctypes.c_void_p(257), 1 << 30, one, None) == 1
+    assert lib.qsa_select_from_scores(ctypes.byref(p), one, one, None, 512, one, None) == 1  # null workspace
