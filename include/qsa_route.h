@@ -56,9 +56,9 @@ extern "C" {
  * global position of local row 0 (cp_rank * S_q for the contiguous layout).
  * Every local position must lie inside the global sequence:
  * query_position_offset + S_q <= n_blocks * compress_ratio + compress_ratio - 1.
- * Supported: H_index a power of two, 1..128; D_index 64 or 128; n_blocks up to
- * 32768; unit last strides, other strides multiples of 8 elements, 16-byte
- * aligned bases. */
+ * Supported: H_index a power of two, 1..128; D_index 64 or 128; token IDs and
+ * the row width within int32; unit last strides, other strides multiples of 8
+ * elements, 16-byte aligned bases. */
 typedef struct qsa_route_problem {
     int64_t B, S_q, H_index, D_index, n_blocks;
     int64_t token_budget, compress_ratio, query_position_offset;

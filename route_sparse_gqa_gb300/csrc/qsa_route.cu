@@ -31,13 +31,18 @@
 // QSA_ERR_TIMEOUT in the status word, the roles wind down, the tensor pipe and
 // the copies drain, and the TMEM is freed.
 //
-// Selection.  One CTA per query row: the row's visible scores become
-// order-preserving 32-bit keys in shared memory, a four-pass radix select
-// (8-bit digits, warp-aggregated histograms) finds the key T of the
-// floor(budget / c)-th best block and how many blocks equal to T to keep
-// (lowest indices first), and a block-wide scan places the chosen blocks in
-// ascending order; each expands to its c token IDs, the incomplete causal
-// tail follows, then -1.
+// Selection.  One CTA per query row.  Each thread loads a contiguous segment
+// of 32 visible scores as order-preserving 32-bit keys into registers (rows
+// of up to 8192 visible blocks stay resident; longer rows are walked in
+// chunks of 8192, re-read from L2 for each pass).  A three-pass radix select
+// with 11-bit digits (shared-memory histograms, conflict-free scans) finds the
+// key T of the floor(budget / c)-th best block and how many blocks equal to T
+// to keep (lowest indices first); one block-wide scan of the per-segment
+// counts then gives every thread the output position of its first chosen
+// block, and a bit mask of its chosen keys is walked in index order, so the
+// chosen blocks come out ascending.  Each expands to its c token IDs, the
+// incomplete causal tail follows, then -1; the row is assembled in shared
+// memory and written with coalesced stores.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -63,7 +68,6 @@ constexpr int kScoreStages = 4;
 constexpr int kMaxIndexDim = 128;
 constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 fp32 columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kMaxSelBlocks = 32768;  // selection keeps a row's keys in shared memory
 
 // Barrier slots.
 enum { kBarQFull, kBarQEmpty, kBarDrain, kBarKFull, kBarKEmpty = kBarKFull + kScoreStages,
@@ -319,29 +323,30 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
 // ------------------------------------------------------------- selection ----
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kKeysPerThread = 32;                          // a thread's contiguous segment of a chunk
+constexpr int64_t kSelChunk = kSelThreads * kKeysPerThread;  // keys held in registers at once
+constexpr int kDigitBins = 2048;                            // 11-bit digits: bits 31-21, 20-10, 9-0
+constexpr int kStageMax = 12288;                            // output rows up to this width are staged
 
 struct SelParams {
     const float *scores;  // [B, S_q, NB]
     const int64_t *seq_len;
     int32_t *ids;  // [B, S_q, W]
-    int64_t S_q, NB, c, offset, n_best, W;
+    int64_t S_q;
+    // Positions, block counts, token IDs and the row width all fit in 31 bits.
+    uint32_t NB, c, offset, n_best, W;
 };
 
-// Shared-memory slot of key i: one pad word every 32 keys, so that both a
-// warp reading 32 consecutive keys and threads walking contiguous 32-key
-// segments hit distinct banks.
-__device__ __forceinline__ int64_t key_slot(int64_t i) { return i + (i >> 5); }
-
-// Order-preserving unsigned key of an fp32 score (larger score, larger key);
-// -0 maps to the key of +0.
+// Order-preserving unsigned key of an fp32 score (larger score, larger key).
+// Adding +0 first turns -0 into +0, so both zeros get one key.
 __device__ __forceinline__ uint32_t score_key(float f) {
-    uint32_t u = __float_as_uint(f);
-    if ((u << 1) == 0u) u = 0u;
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
-// Exclusive block-wide prefix sum of one 32-bit value per thread.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t *warp_tot) {
+// Block-wide exclusive prefix sum of one 32-bit value per thread; `total` gets
+// the sum over the block.  Contains two barriers.
+__device__ __forceinline__ uint32_t block_scan(uint32_t x, uint32_t *warp_tot, uint32_t &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t incl = x;
 #pragma unroll
@@ -351,119 +356,189 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t x, uint32_t *w
     }
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
-    uint32_t before = 0;
-    for (int w = 0; w < warp; ++w) before += warp_tot[w];
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) {
+        const uint32_t t = warp_tot[w];
+        before += w < warp ? t : 0u;
+        all += t;
+    }
     __syncthreads();
+    total = all;
     return before + incl - x;
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const SelParams p) {
-    extern __shared__ uint32_t keys[];  // key_slot(nvis) words
-    __shared__ uint32_t hist[256];
+// Given a digit histogram, finds the digit d holding the remaining-th largest
+// key (counting from the top bin) and how many keys of bin d that rank needs.
+// Warp w owns kBinsPerWarp consecutive bins in best-first order; its lane l
+// reads bins 2047 - (kBinsPerWarp w + 32 j + l), so every read is
+// conflict-free, and warp scans give each bin's count of better keys.
+constexpr int kBinsPerWarp = kDigitBins / kSelWarps;
+__device__ __forceinline__ void find_digit(const uint32_t *hist, uint32_t remaining, uint32_t *warp_tot,
+                                           uint32_t *s_digit, uint32_t *s_rem) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int J = kBinsPerWarp / 32;
+    uint32_t cnt[J], excl[J], run = 0;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        cnt[j] = hist[kDigitBins - 1 - (kBinsPerWarp * warp + 32 * j + lane)];
+        uint32_t incl = cnt[j];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        excl[j] = run + incl - cnt[j];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) warp_tot[warp] = run;
+    __syncthreads();
+    uint32_t base = 0;
+#pragma unroll
+    for (int w = 0; w < kSelWarps; ++w) base += w < warp ? warp_tot[w] : 0u;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint32_t e = base + excl[j];
+        if (e < remaining && remaining <= e + cnt[j]) {
+            *s_digit = (uint32_t)(kDigitBins - 1 - (kBinsPerWarp * warp + 32 * j + lane));
+            *s_rem = remaining - e;
+        }
+    }
+    __syncthreads();
+}
+
+// A load the compiler may not repeat (the loaded keys are meant to stay in
+// registers through every pass, not to be re-read from memory at each use).
+__device__ __forceinline__ float load_once(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// Keys of chunk ch (blocks ch * kSelChunk ..) for this thread's segment;
+// returns how many of its kKeysPerThread slots hold visible blocks.
+__device__ __forceinline__ int load_segment(const float *srow, uint32_t nvis, uint32_t ch,
+                                            uint32_t (&k)[kKeysPerThread]) {
+    const uint32_t i0 = ch * (uint32_t)kSelChunk + threadIdx.x * kKeysPerThread;
+    const int n = i0 >= nvis ? 0 : (int)min(nvis - i0, (uint32_t)kKeysPerThread);
+#pragma unroll
+    for (int j = 0; j < kKeysPerThread; ++j) k[j] = j < n ? score_key(load_once(srow + i0 + j)) : 0u;
+    return n;
+}
+
+__device__ __forceinline__ void clear_hist(uint32_t *hist) {
+#pragma unroll
+    for (int i = threadIdx.x; i < kDigitBins / 4; i += kSelThreads)
+        reinterpret_cast<uint4 *>(hist)[i] = make_uint4(0, 0, 0, 0);
+}
+
+// Grid (S_q, B): one CTA per query row.
+__global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams p) {
+    extern __shared__ __align__(16) int32_t stage[];  // the output row, when it is staged
+    __shared__ __align__(16) uint32_t hist[kDigitBins];
     __shared__ uint32_t warp_tot[kSelWarps];
     __shared__ uint32_t s_digit, s_remaining;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t row = blockIdx.x;
-    const int64_t b = row / p.S_q, t = row % p.S_q;
-    const int64_t tg = p.offset + t;
-    int32_t *out = p.ids + row * p.W;
-    int64_t n_out = 0;
-    if (tg < p.seq_len[b]) {
-        const int64_t nvis = min(p.NB, (tg + 1) / p.c);
-        const int64_t n_sel = min(nvis, p.n_best);
+    const int tid = threadIdx.x;
+    const uint32_t t = blockIdx.x, b = blockIdx.y;
+    const int64_t row = (int64_t)b * p.S_q + t;
+    const uint32_t tg = p.offset + t;
+    int32_t *gout = p.ids + row * p.W;
+    const bool staged = p.W <= (uint32_t)kStageMax;
+    int32_t *out = staged ? stage : gout;
+    uint32_t n_out = 0;
+    if ((int64_t)tg < p.seq_len[b]) {
+        const uint32_t nvis = min(p.NB, (tg + 1) / p.c);
+        const uint32_t n_sel = min(nvis, p.n_best);
         n_out = n_sel * p.c + (tg + 1 - nvis * p.c);
         if (nvis <= p.n_best) {
             // Every visible block is chosen: the row is dense causal, 0 .. tg.
-            for (int64_t i = tid; i < n_out; i += kSelThreads) out[i] = (int32_t)i;
+            for (uint32_t i = tid; i < n_out; i += kSelThreads) out[i] = (int32_t)i;
         } else {
             const float *srow = p.scores + row * p.NB;
-            for (int64_t i = tid; i < nvis; i += kSelThreads) keys[key_slot(i)] = score_key(__ldg(srow + i));
-            __syncthreads();
-            // Radix select, most significant digit first: find the key T of the
-            // n_best-th best block and how many blocks equal to T are kept.
-            uint32_t prefix = 0, mask = 0, remaining = (uint32_t)p.n_best;
+            const uint32_t n_chunks = (nvis + (uint32_t)kSelChunk - 1) / (uint32_t)kSelChunk;
+            const bool resident = n_chunks == 1;  // the whole row stays in registers
+            uint32_t k[kKeysPerThread];
+            int n = resident ? load_segment(srow, nvis, 0, k) : 0;
+            // Three radix passes, most significant digit first, find the key T of
+            // the n_best-th best block and how many blocks equal to T are kept.
+            uint32_t prefix = 0, mask = 0, remaining = p.n_best;
 #pragma unroll 1
-            for (int shift = 24; shift >= 0; shift -= 8) {
-                hist[tid] = 0;
+            for (int pass = 0; pass < 3; ++pass) {
+                const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+                const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
+                clear_hist(hist);
                 __syncthreads();
-                for (int64_t base = 0; base < nvis; base += kSelThreads) {
-                    const int64_t i = base + tid;
-                    uint32_t k = 0;
-                    bool m = false;
-                    if (i < nvis) {
-                        k = keys[key_slot(i)];
-                        m = (k & mask) == prefix;
-                    }
-                    const uint32_t act = __ballot_sync(0xffffffffu, m);
-                    if (m) {
-                        const uint32_t d = (k >> shift) & 255u;
-                        const uint32_t peers = __match_any_sync(act, d);
-                        if ((peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+                for (uint32_t ch = 0; ch < n_chunks; ++ch) {
+                    if (!resident) n = load_segment(srow, nvis, ch, k);
+                    if (pass == 0) {
+#pragma unroll
+                        for (int j = 0; j < kKeysPerThread; ++j)
+                            if (j < n) atomicAdd(&hist[k[j] >> 21], 1u);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kKeysPerThread; ++j)
+                            if (j < n && (k[j] & mask) == prefix) atomicAdd(&hist[(k[j] >> shift) & dmask], 1u);
                     }
                 }
                 __syncthreads();
-                if (warp == 0) {
-                    // Lane l holds digits 255 - 8l .. 248 - 8l (best first).
-                    uint32_t cnt[8], sum = 0;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        cnt[j] = hist[255 - 8 * lane - j];
-                        sum += cnt[j];
-                    }
-                    uint32_t incl = sum;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    uint32_t acc = incl - sum;
-                    if (acc < remaining && remaining <= incl) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (acc + cnt[j] >= remaining) {
-                                s_digit = (uint32_t)(255 - 8 * lane - j);
-                                s_remaining = remaining - acc;
-                                break;
-                            }
-                            acc += cnt[j];
-                        }
-                    }
-                }
-                __syncthreads();
+                find_digit(hist, remaining, warp_tot, &s_digit, &s_remaining);
                 prefix |= s_digit << shift;
-                mask |= 255u << shift;
+                mask |= dmask << shift;
                 remaining = s_remaining;
             }
             const uint32_t T = prefix, need = remaining;  // keep every key > T and the first `need` keys == T
-            // Contiguous segments of 32 * m keys per thread, in index order.
-            const int64_t seg = ((nvis + kSelThreads - 1) / kSelThreads + 31) & ~int64_t(31);
-            const int64_t i0 = min(nvis, tid * seg), i1 = min(nvis, i0 + seg);
-            uint32_t gt = 0, eq = 0;
-            for (int64_t i = i0; i < i1; ++i) {
-                const uint32_t k = keys[key_slot(i)];
-                gt += k > T;
-                eq += k == T;
-            }
-            // gt and eq stay below 2^16 (NB <= 32768): scan both in one word.
-            const uint32_t before = block_exclusive_scan(gt | (eq << 16), warp_tot);
-            const uint32_t gt_before = before & 0xFFFFu, eq_before = before >> 16;
-            uint32_t pos = gt_before + min(eq_before, need), eq_seen = eq_before;
-            for (int64_t i = i0; i < i1; ++i) {
-                const uint32_t k = keys[key_slot(i)];
-                bool take = k > T;
-                if (k == T) take = eq_seen++ < need;
-                if (take && pos < (uint32_t)n_sel) {
-                    int32_t *dst = out + (int64_t)pos * p.c;
-                    for (int64_t j = 0; j < p.c; ++j) dst[j] = (int32_t)(i * p.c + j);
+            // Place the chosen blocks in index order: one block-wide scan of the
+            // per-segment counts (key > T, key == T) per chunk gives each thread
+            // its first output position and its rank among the ties; a bit mask
+            // of the segment's chosen keys is then walked set bit by set bit.
+            uint32_t sel_run = 0, eq_run = 0;
+            const bool vec4 = staged && p.c == 4;  // whole 16-byte stores into the staged row
+            for (uint32_t ch = 0; ch < n_chunks; ++ch) {
+                if (!resident) n = load_segment(srow, nvis, ch, k);
+                uint32_t gt_mask = 0, eq_mask = 0;  // bit j: key j of the segment
+#pragma unroll
+                for (int j = 0; j < kKeysPerThread; ++j) {
+                    gt_mask |= (uint32_t)(j < n && k[j] > T) << j;
+                    eq_mask |= (uint32_t)(j < n && k[j] == T) << j;
+                }
+                const uint32_t eq = __popc(eq_mask);
+                uint32_t tot;
+                const uint32_t ex = block_scan(__popc(gt_mask) | (eq << 16), warp_tot, tot);
+                const uint32_t eq_rank = eq_run + (ex >> 16);  // ties before this segment
+                const uint32_t keep = eq_rank >= need ? 0u : min(eq, need - eq_rank);
+                while ((uint32_t)__popc(eq_mask) > keep) eq_mask &= ~(1u << (31 - __clz(eq_mask)));
+                uint32_t take = gt_mask | eq_mask;
+                uint32_t pos = sel_run + (ex & 0xFFFFu) + min(eq_rank, need) - min(eq_run, need);
+                const uint32_t i0 = ch * (uint32_t)kSelChunk + tid * kKeysPerThread;
+                while (take) {
+                    const uint32_t j = (uint32_t)(__ffs(take) - 1);
+                    take &= take - 1;
+                    if (pos < n_sel) {
+                        const int32_t first = (int32_t)((i0 + j) * p.c);
+                        if (vec4) {
+                            reinterpret_cast<int4 *>(out)[pos] = make_int4(first, first + 1, first + 2, first + 3);
+                        } else {
+                            int32_t *dst = out + (size_t)pos * p.c;
+                            for (uint32_t e = 0; e < p.c; ++e) dst[e] = first + (int32_t)e;
+                        }
+                    }
                     ++pos;
                 }
+                const uint32_t eq_tot = tot >> 16;
+                sel_run += (tot & 0xFFFFu) + min(eq_run + eq_tot, need) - min(eq_run, need);
+                eq_run += eq_tot;
             }
             // Causal tail: the tokens of the incomplete block.
-            for (int64_t i = tid; i < tg + 1 - nvis * p.c; i += kSelThreads)
+            for (uint32_t i = tid; i < tg + 1 - nvis * p.c; i += kSelThreads)
                 out[n_sel * p.c + i] = (int32_t)(nvis * p.c + i);
         }
     }
-    for (int64_t i = n_out + tid; i < p.W; i += kSelThreads) out[i] = -1;
+    if (staged) {
+        __syncthreads();
+        for (uint32_t i = tid; i < p.W; i += kSelThreads) gout[i] = i < n_out ? stage[i] : -1;
+    } else {
+        for (uint32_t i = n_out + tid; i < p.W; i += kSelThreads) gout[i] = -1;
+    }
 }
 
 // --------------------------------------------------------------- host side ----
@@ -497,11 +572,10 @@ qsa_status validate_route(const qsa_route_problem *p) {
                           (long long)p->H_index);
     if (p->D_index != 64 && p->D_index != kMaxIndexDim)
         return route_fail(QSA_ERR_UNSUPPORTED, "D_index=%lld: 64 or 128 is supported", (long long)p->D_index);
-    if (p->n_blocks > kMaxSelBlocks)
-        return route_fail(QSA_ERR_UNSUPPORTED, "n_blocks=%lld exceeds %d", (long long)p->n_blocks, kMaxSelBlocks);
     if (p->n_blocks * c + c > 2147483647LL || p->token_budget + c - 1 > 2147483647LL)
         return route_fail(QSA_ERR_UNSUPPORTED, "token IDs or the row width exceed int32");
-    if (p->B * p->S_q > 2147483647LL) return route_fail(QSA_ERR_UNSUPPORTED, "B * S_q exceeds 2^31 - 1");
+    if (p->B > 65535 || p->S_q > 2147483647LL)
+        return route_fail(QSA_ERR_UNSUPPORTED, "B up to 65535 and S_q up to 2^31 - 1 are supported");
     if (p->q_stride[3] != 1 || p->k_stride[2] != 1)
         return route_fail(QSA_ERR_UNSUPPORTED, "index_queries and compressed_keys need a unit last stride");
     for (int i = 0; i < 3; ++i)
@@ -605,22 +679,19 @@ qsa_status launch_select(const qsa_route_problem *pr, const float *scores, const
     p.seq_len = seq_len;
     p.ids = ids;
     p.S_q = pr->S_q;
-    p.NB = pr->n_blocks;
-    p.c = pr->compress_ratio;
-    p.offset = pr->query_position_offset;
-    p.n_best = pr->token_budget / pr->compress_ratio;
-    p.W = pr->token_budget + pr->compress_ratio - 1;
-    // Keys of the longest visible prefix any row can have.
-    const int64_t max_vis = std::min<int64_t>(p.NB, (p.offset + p.S_q) / p.c);
-    const size_t smem = (size_t)(max_vis + (max_vis >> 5) + 1) * sizeof(uint32_t);
+    p.NB = (uint32_t)pr->n_blocks;
+    p.c = (uint32_t)pr->compress_ratio;
+    p.offset = (uint32_t)pr->query_position_offset;
+    p.n_best = (uint32_t)(pr->token_budget / pr->compress_ratio);
+    p.W = (uint32_t)(pr->token_budget + pr->compress_ratio - 1);
+    const size_t smem = p.W <= (uint32_t)kStageMax ? (size_t)p.W * sizeof(int32_t) : 0;
     if (smem > 48 * 1024) {
         qsa_status st = cuda_status(
             cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
             "cudaFuncSetAttribute");
         if (st != QSA_OK) return st;
     }
-    const int64_t rows = pr->B * pr->S_q;
-    select_kernel<<<(unsigned)rows, kSelThreads, smem, stream>>>(p);
+    select_kernel<<<dim3((unsigned)pr->S_q, (unsigned)pr->B), kSelThreads, smem, stream>>>(p);
     return cuda_status(cudaGetLastError(), "selection kernel launch");
 }
 

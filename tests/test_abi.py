@@ -160,7 +160,7 @@ def good_route_problem(**kw):
     ({"H_index": 256}, 2),
     ({"D_index": 256}, 2),
     ({"D_index": 96}, 2),
-    ({"n_blocks": 40000, "S_q": 160000}, 2),
+    ({"n_blocks": 600_000_000}, 2),         # token IDs past int32
     ({"q_stride": (100 * 32 * 128, 32 * 128, 128, 2)}, 2),
     ({"k_stride": (25 * 128, 132, 1)}, 2),
 ])

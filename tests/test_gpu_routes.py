@@ -185,6 +185,9 @@ def _quantised_scores(rng, B, S_q, NB, step):
     (1, 300, 1, 5, 0, (300,), 300, 1.0),
     (2, 200, 7, 20, 100, (300, 250), 300, 0.5),
     (1, 64, 4, 2048, 32704, (32768,), 32768, 1e-3),    # full-size rows: 8176+ visible blocks, 512 chosen
+    (1, 64, 4, 2048, 32704, (32768,), 32768, 8.0),     # most scores tie at 0: thousands of keys share one bin
+    (1, 32, 4, 2048, 79968, (80000,), 80000, 1e-3),    # 20000 visible blocks: rows walked in chunks
+    (1, 32, 4, 16384, 79968, (80000,), 80000, 8.0),    # 4096 chosen, ties, a row too wide to stage
     (1, 50, 4, 3, 0, (50,), 50, 0.5),                  # budget < c: only the causal tails
     (1, 40, 4, 16, 0, (0,), 40, 0.5),                  # every row padding
 ])
