@@ -13,6 +13,13 @@ device->host copies of O, LSE, dQ, dK, dV are inside its timed region.
 ``--impl reference`` times the fp64 CPU oracle (the only reference this method
 has) on a bounded sample of the same workload, on the host cores.
 
+``--route-producer`` measures the route producer instead (compressed-block
+index scores + top-k selection, ``select_qsa_token_ids``) on the training-step
+index workload (B=1, S=32768, H_index=32, D_index=128, c=4, budget 2048): one
+step = the score kernel and the selection kernel through the C ABI; ``value`` is
+useful TFLOP/s of the scoring (2*H*D per visible (row, block) pair) over the
+whole step.  With ``--impl reference`` it times the oracle on sampled rows.
+
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 path needs no exchange); the barrier and the max-over-ranks timing use
 torch.distributed, nothing on the data path does.
@@ -484,6 +491,244 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+ROUTE_METRIC = "QSA route producer (index scores + top-k block selection) useful TFLOP/s on 1 GB300"
+ROUTE_WORKLOAD = 3  # index-train-step
+
+
+def route_work(w, lengths):
+    """Visible (row, block) pairs of live rows and the scoring FLOP on them."""
+    tg = np.arange(w.S_q, dtype=np.int64) + w.offset
+    pairs = 0
+    for L in lengths:
+        live = tg < int(L)
+        pairs += int(np.minimum((tg[live] + 1) // w.c, w.n_blocks).sum())
+    rows = int(sum(min(w.S_q, max(0, int(L) - w.offset)) for L in lengths))
+    return pairs, 2 * w.H * w.D * pairs, rows
+
+
+def run_route_producer(args):
+    import ctypes
+
+    import torch
+    import torch.distributed as dist
+
+    import route_sparse_gqa_gb300 as qsa
+    from route_sparse_gqa_gb300 import _abi
+    from route_sparse_gqa_gb300 import build as qbuild
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qbuild.build()
+    case = W.make_index_case(ROUTE_WORKLOAD)
+    w = case.workload
+    bf = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)  # noqa: E731
+    q, k = bf(case.q).to(dev), bf(case.k).to(dev)
+    lens = torch.from_numpy(case.lengths).to(dev)
+    prob, qq, kk = qsa.routes._problem(q, k, w.budget, w.c, w.offset, w.S_global)
+    lib = _abi.load()
+    ws_bytes = lib.qsa_route_workspace_bytes(ctypes.byref(prob))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    scores_ptr = ws.data_ptr() + 512  # the workspace's score tensor
+    W_ = w.budget + w.c - 1
+    ids = torch.empty((w.B, w.S_q, W_), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    pairs, flop, live_rows = route_work(w, case.lengths)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        _abi.check(lib.qsa_index_scores(ctypes.byref(prob), qq.data_ptr(), kk.data_ptr(), lens.data_ptr(),
+                                        ws.data_ptr(), ws_bytes, scores_ptr, stream))
+        if ev:
+            ev[1].record()
+        _abi.check(lib.qsa_select_from_scores(ctypes.byref(prob), scores_ptr, lens.data_ptr(), ws.data_ptr(),
+                                              ws_bytes, ids.data_ptr(), stream))
+        if ev:
+            ev[2].record()
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    _abi.check(lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream)))
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            step(events[i])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    per = np.array([[events[i][0].elapsed_time(events[i][1]), events[i][1].elapsed_time(events[i][2])]
+                    for i in range(args.steps)])
+    score_ms, sel_ms = (float(x) for x in per.mean(0))
+    step_ms = max_over_ranks(score_ms + sel_ms, dev)
+    value = job_tflops(flop, world, step_ms)
+    _abi.check(lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream)))
+
+    # End to end through the public binding with pinned host buffers: H2D of the
+    # index states and lengths, the producer, D2H of the route rows.
+    hq = bf(case.q).pin_memory()
+    hk = bf(case.k).pin_memory()
+    hl = torch.from_numpy(case.lengths).pin_memory()
+    hids = torch.empty((w.B, w.S_q, W_), dtype=torch.int32).pin_memory()
+    dq_, dk_, dl_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(lens)
+
+    def e2e_step():
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dl_.copy_(hl, non_blocking=True)
+        out = qsa.select_qsa_token_ids(dq_, dk_, dl_, w.budget, w.c, query_position_offset=w.offset,
+                                       global_sequence_length=w.S_global)
+        hids.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(3, min(args.steps, 10))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n_e2e):
+        e2e_step()
+    t1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / n_e2e, dev)
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hl.numel() * 8
+    d2h = hids.numel() * 4
+    e2e = {"value": round(job_tflops(flop, world, e2e_ms), 3), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+           "pipeline": "none: copies and compute in sequence on one stream"}
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops"])
+    score_tf = flop / (score_ms * 1e-3) / 1e12
+    sel_bytes = 4 * pairs + 4 * W_ * w.B * w.S_q + 8 * w.B  # scores read once, route rows written, lengths
+    sel_gbs = sel_bytes / (sel_ms * 1e-3) / 1e9
+    kernels = {
+        "index_score_kernel": {"bound": "tensor", "achieved": round(score_tf, 2), "peak": tc_peak,
+                               "unit": "TFLOP/s", "frac": round(score_tf / tc_peak, 4), "launch_ms": round(score_ms, 4),
+                               "algorithmic_flop_per_launch": flop, "traffic": recorded_traffic("index_score_kernel")},
+        "select_kernel": {"bound": "hbm", "achieved": round(sel_gbs, 1), "peak": hbm, "unit": "GB/s",
+                          "frac": round(sel_gbs / hbm, 4), "launch_ms": round(sel_ms, 4),
+                          "algorithmic_bytes_per_launch": sel_bytes, "traffic": recorded_traffic("select_kernel")},
+    }
+    dom = "select_kernel" if sel_ms >= score_ms else "index_score_kernel"
+    roofline = dict(kernels[dom])
+    roofline["kernel"] = dom
+    roofline["peak_source"] = f"{peak_src} MEASURED_PEAKS.json" if peak_src == "measured" else "fallback"
+    cpu = run_route_cpu_baseline(case, w, flop, live_rows, args) if (rank == 0 and world == 1 and
+                                                                     not args.no_cpu_baseline) else None
+    line = {
+        "metric": ROUTE_METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{w.name}: {w.summary}",
+            "step": "index scores (tcgen05) + top-k block selection and expansion",
+            "parallelism": f"replicas x{world}",
+            "l2": "flushed before every timed step (256 MiB write outside the events)",
+            "visible_pairs": pairs,
+            "useful_flop_per_step": flop,
+        },
+        "breakdown_ms": {"index_scores": round(score_ms, 4), "selection": round(sel_ms, 4)},
+        "roofline": roofline,
+        "kernels": kernels,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+ROUTE_GROUP = 16  # contiguous query rows per oracle call (the oracle's threads split a call's rows)
+
+
+def route_oracle_sample(case, w, n_rows: int):
+    """Groups of ROUTE_GROUP contiguous live query rows of batch row 0, evenly
+    spaced over the sequence, for the route-producer oracle."""
+    live = min(w.S_q, int(case.lengths[0]) - w.offset)
+    n_groups = max(1, min(n_rows // ROUTE_GROUP, live // ROUTE_GROUP))
+    starts = np.linspace(0, live - ROUTE_GROUP, n_groups).astype(np.int64)
+    rows = (starts[:, None] + np.arange(ROUTE_GROUP)[None, :]).reshape(-1)
+    tg = rows + w.offset
+    pairs = int(np.minimum((tg + 1) // w.c, w.n_blocks).sum())
+    return starts, rows, pairs
+
+
+def time_route_oracle(case, w, starts):
+    import oracle
+
+    f64 = lambda bits: W.bf16_bits_to_f32(bits).astype(np.float64)  # noqa: E731
+    kd = f64(case.k[:1])
+    qs = [f64(case.q[:1, s:s + ROUTE_GROUP]) for s in starts]
+    t0 = time.perf_counter()
+    for s, qd in zip(starts, qs):
+        oracle.select_qsa_token_ids(qd, kd, case.lengths[:1], w.budget, w.c, w.offset + int(s))
+    return time.perf_counter() - t0
+
+
+def run_route_cpu_baseline(case, w, flop, live_rows, args):
+    import oracle
+
+    oracle.build()
+    starts, rows, pairs = route_oracle_sample(case, w, args.route_rows)
+    secs = time_route_oracle(case, w, starts)
+    return {"value": round(2 * w.H * w.D * pairs / secs / 1e12, 6), "unit": UNIT,
+            "cores": min(oracle.omp_threads(), ROUTE_GROUP), "kind": "oracle", "seconds": round(secs, 2),
+            "sample": f"{starts.size} groups of {ROUTE_GROUP} contiguous query rows of batch row 0, evenly spaced "
+                      f"({pairs} visible blocks), scores + selection in fp64"}
+
+
+def run_route_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    case = W.make_index_case(ROUTE_WORKLOAD)
+    w = case.workload
+    starts, rows, pairs = route_oracle_sample(case, w, args.route_rows)
+    for _ in range(args.warmup):
+        time_route_oracle(case, w, starts[:1])
+    secs = [time_route_oracle(case, w, starts) for _ in range(args.steps)]
+    total = sum(secs)
+    value = 2 * w.H * w.D * pairs * args.steps / total / 1e12
+    sample = (f"{starts.size} groups of {ROUTE_GROUP} contiguous query rows of batch row 0, evenly spaced "
+              f"({pairs} visible blocks) per step, scores + selection in fp64")
+    line = {
+        "impl": "reference", "metric": ROUTE_METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.summary}", "step": "oracle scores + selection on a bounded sample",
+                   "parallelism": "CPU threads (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": min(oracle.omp_threads(), ROUTE_GROUP),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -494,10 +739,15 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=6144, help="query rows in the CPU-baseline oracle sample")
     ap.add_argument("--ref-rows", type=int, default=160, help="query rows per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--route-producer", action="store_true",
+                    help="measure the route producer (index scores + top-k selection) instead of the attention")
+    ap.add_argument("--route-rows", type=int, default=256, help="query rows in the route-producer oracle sample")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
-    if args.impl == "reference":
+    if args.route_producer:
+        (run_route_reference if args.impl == "reference" else run_route_producer)(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -78,3 +78,30 @@ def test_long_rows(index):
     assert np.all(last == q)
     if index == 3:
         assert w.B * w.S_q * w.S_kv == 2**32
+
+
+def test_index_workloads_shapes_and_seeding():
+    c0 = W.make_index_case(0)
+    c1 = W.make_index_case(0)
+    w = c0.workload
+    assert c0.q.shape == (w.B, w.S_q, w.H, w.D) and c0.k.shape == (w.B, w.n_blocks, 1, w.D)
+    assert np.array_equal(c0.q, c1.q) and np.array_equal(c0.k, c1.k)
+    assert list(c0.lengths) == list(w.lengths)
+    for iw in W.INDEX_WORKLOADS:  # every local position lies inside the global sequence
+        assert iw.offset + iw.S_q <= iw.n_blocks * iw.c + iw.c - 1
+        assert max(iw.lengths) <= iw.S_global
+
+
+def test_bench_route_work_counts_visible_pairs():
+    import bench
+
+    w = W.IndexWorkload(9, "t", 2, 37, 60, 20, 4, 64, 3, 6, (50, 30), "t")
+    pairs, flop, rows = bench.route_work(w, w.lengths)
+    want = 0
+    for L in w.lengths:
+        for t in range(w.S_q):
+            tg = w.offset + t
+            if tg < L:
+                want += min((tg + 1) // w.c, w.n_blocks)
+    assert pairs == want and flop == 2 * w.H * w.D * want
+    assert rows == min(w.S_q, 50 - 20) + min(w.S_q, 30 - 20)
