@@ -135,10 +135,23 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_source_hash() -> str:
+# Sources each profiled kernel is built from: a recorded DRAM traffic figure stays
+# valid until one of them changes.
+KERNEL_SOURCES = {
+    "qsa_forward": ["qsa_fwd_tc.cu", "qsa_tc_host.cu", "qsa_tc_ptx.cuh", "qsa_queue.cuh", "qsa_tc.cuh", "qsa_internal.cuh"],
+    "qsa_backward": ["qsa_bwd_tc.cu", "qsa_tc_host.cu", "qsa_tc_ptx.cuh", "qsa_queue.cuh", "qsa_tc.cuh", "qsa_internal.cuh"],
+    "index_score_kernel": ["qsa_route.cu", "qsa_tc_host.cu", "qsa_tc_ptx.cuh", "qsa_queue.cuh", "qsa_tc.cuh",
+                           "qsa_internal.cuh"],
+    "select_kernel": ["qsa_route.cu"],
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of the kernel's source files (every CUDA source when `kernel` is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "route_sparse_gqa_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES.get(kernel) if kernel else None
+    for name in sorted(names or os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -146,7 +159,7 @@ def kernel_source_hash() -> str:
 
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
-    taken on the current kernel sources."""
+    taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -154,7 +167,7 @@ def recorded_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     entry = rec.get(kernel)
-    if not entry or entry.get("source_hash") != kernel_source_hash():
+    if not entry or entry.get("source_hash") != kernel_source_hash(kernel):
         return None
     return entry.get("bytes_per_launch")
 
