@@ -327,6 +327,7 @@ constexpr int kKeysPerThread = 32;                          // a thread's contig
 constexpr int64_t kSelChunk = kSelThreads * kKeysPerThread;  // keys held in registers at once
 constexpr int kDigitBins = 2048;                            // 11-bit digits: bits 31-21, 20-10, 9-0
 constexpr int kStageMax = 12288;                            // output rows up to this width are staged
+constexpr int kCandCap = 2048;                              // keys of one first-pass bin kept in shared memory
 
 struct SelParams {
     const float *scores;  // [B, S_q, NB]
@@ -369,13 +370,14 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t x, uint32_t *warp_tot, u
 }
 
 // Given a digit histogram, finds the digit d holding the remaining-th largest
-// key (counting from the top bin) and how many keys of bin d that rank needs.
+// key (counting from the top bin), how many keys of bin d that rank needs, and
+// how many keys bin d holds.
 // Warp w owns kBinsPerWarp consecutive bins in best-first order; its lane l
 // reads bins 2047 - (kBinsPerWarp w + 32 j + l), so every read is
 // conflict-free, and warp scans give each bin's count of better keys.
 constexpr int kBinsPerWarp = kDigitBins / kSelWarps;
 __device__ __forceinline__ void find_digit(const uint32_t *hist, uint32_t remaining, uint32_t *warp_tot,
-                                           uint32_t *s_digit, uint32_t *s_rem) {
+                                           uint32_t *s_digit, uint32_t *s_rem, uint32_t *s_cnt) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int J = kBinsPerWarp / 32;
     uint32_t cnt[J], excl[J], run = 0;
@@ -402,6 +404,7 @@ __device__ __forceinline__ void find_digit(const uint32_t *hist, uint32_t remain
         if (e < remaining && remaining <= e + cnt[j]) {
             *s_digit = (uint32_t)(kDigitBins - 1 - (kBinsPerWarp * warp + 32 * j + lane));
             *s_rem = remaining - e;
+            *s_cnt = cnt[j];
         }
     }
     __syncthreads();
@@ -415,15 +418,42 @@ __device__ __forceinline__ float load_once(const float *p) {
     return v;
 }
 
+__device__ __forceinline__ float4 load_once4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
 // Keys of chunk ch (blocks ch * kSelChunk ..) for this thread's segment;
-// returns how many of its kKeysPerThread slots hold visible blocks.
+// returns how many of its kKeysPerThread slots hold visible blocks.  A full
+// segment of a 16-byte aligned row is read with 16-byte loads: the 32 lanes of
+// a warp read 32 different 128-byte lines per instruction, so wide loads cut
+// the L1 transactions fourfold.
 __device__ __forceinline__ int load_segment(const float *srow, uint32_t nvis, uint32_t ch,
-                                            uint32_t (&k)[kKeysPerThread]) {
+                                            uint32_t (&k)[kKeysPerThread], bool aligned16) {
     const uint32_t i0 = ch * (uint32_t)kSelChunk + threadIdx.x * kKeysPerThread;
     const int n = i0 >= nvis ? 0 : (int)min(nvis - i0, (uint32_t)kKeysPerThread);
+    if (aligned16 && n == kKeysPerThread) {
 #pragma unroll
-    for (int j = 0; j < kKeysPerThread; ++j) k[j] = j < n ? score_key(load_once(srow + i0 + j)) : 0u;
+        for (int j = 0; j < kKeysPerThread; j += 4) {
+            const float4 v = load_once4(srow + i0 + j);
+            k[j] = score_key(v.x);
+            k[j + 1] = score_key(v.y);
+            k[j + 2] = score_key(v.z);
+            k[j + 3] = score_key(v.w);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kKeysPerThread; ++j) k[j] = j < n ? score_key(load_once(srow + i0 + j)) : 0u;
+    }
     return n;
+}
+
+// Words of the selection kernel's dynamic shared region.
+inline size_t select_smem_words(uint32_t W) {
+    const size_t transpose = kSelChunk + kSelChunk / 32;
+    const size_t later = 2 * kDigitBins + kCandCap + (W <= (uint32_t)kStageMax ? W : 0);
+    return transpose > later ? transpose : later;
 }
 
 __device__ __forceinline__ void clear_hist(uint32_t *hist) {
@@ -434,10 +464,15 @@ __device__ __forceinline__ void clear_hist(uint32_t *hist) {
 
 // Grid (S_q, B): one CTA per query row.
 __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams p) {
-    extern __shared__ __align__(16) int32_t stage[];  // the output row, when it is staged
-    __shared__ __align__(16) uint32_t hist[kDigitBins];
+    // One dynamic region, used in turn: a padded transposition buffer for the
+    // row's keys while they load; then two digit histograms, the candidate keys
+    // and the staged output row (select_smem_words gives its size).
+    extern __shared__ __align__(16) uint32_t region[];
+    uint32_t(*hist)[kDigitBins] = reinterpret_cast<uint32_t(*)[kDigitBins]>(region);
+    uint32_t *cand = region + 2 * kDigitBins;  // keys of the first pass's chosen bin
+    int32_t *stage = reinterpret_cast<int32_t *>(region + 2 * kDigitBins + kCandCap);  // the output row
     __shared__ uint32_t warp_tot[kSelWarps];
-    __shared__ uint32_t s_digit, s_remaining;
+    __shared__ uint32_t s_digit, s_remaining, s_count, s_ncand;
     const int tid = threadIdx.x;
     const uint32_t t = blockIdx.x, b = blockIdx.y;
     const int64_t row = (int64_t)b * p.S_q + t;
@@ -458,33 +493,87 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
             const uint32_t n_chunks = (nvis + (uint32_t)kSelChunk - 1) / (uint32_t)kSelChunk;
             const bool resident = n_chunks == 1;  // the whole row stays in registers
             uint32_t k[kKeysPerThread];
-            int n = resident ? load_segment(srow, nvis, 0, k) : 0;
+            const bool a16 = (reinterpret_cast<uintptr_t>(srow) & 15u) == 0;
+            int n = 0;
+            if (resident) {
+                // Coalesced loads (a warp reads 32 consecutive scores), transposed
+                // through shared memory into each thread's contiguous segment; one
+                // pad word every 32 keys keeps both sides free of bank conflicts.
+#pragma unroll
+                for (int j = 0; j < kKeysPerThread; ++j) {
+                    const uint32_t i = (uint32_t)j * kSelThreads + tid;
+                    if (i < nvis) region[i + (i >> 5)] = score_key(load_once(srow + i));
+                }
+                __syncthreads();
+                const uint32_t i0 = (uint32_t)tid * kKeysPerThread;
+                n = i0 >= nvis ? 0 : (int)min(nvis - i0, (uint32_t)kKeysPerThread);
+#pragma unroll
+                for (int j = 0; j < kKeysPerThread; ++j) k[j] = j < n ? region[i0 + tid + j] : 0u;
+                __syncthreads();  // the region becomes the histograms
+            }
             // Three radix passes, most significant digit first, find the key T of
             // the n_best-th best block and how many blocks equal to T are kept.
+            // The passes alternate between two histograms (the idle one is cleared
+            // during the other's pass).  After the first pass, the keys of its chosen
+            // bin are gathered into shared memory when they fit, and the other two
+            // passes read only those.
             uint32_t prefix = 0, mask = 0, remaining = p.n_best;
+            bool use_cand = false;
+            clear_hist(hist[0]);
+            clear_hist(hist[1]);
+            if (tid == 0) s_ncand = 0;
+            __syncthreads();
 #pragma unroll 1
             for (int pass = 0; pass < 3; ++pass) {
                 const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
                 const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
-                clear_hist(hist);
-                __syncthreads();
-                for (uint32_t ch = 0; ch < n_chunks; ++ch) {
-                    if (!resident) n = load_segment(srow, nvis, ch, k);
-                    if (pass == 0) {
+                uint32_t *h = hist[pass & 1];
+                if (use_cand) {
+                    for (uint32_t i = tid; i < s_ncand; i += kSelThreads) {
+                        const uint32_t kc = cand[i];
+                        if ((kc & mask) == prefix) atomicAdd(&h[(kc >> shift) & dmask], 1u);
+                    }
+                } else {
+                    for (uint32_t ch = 0; ch < n_chunks; ++ch) {
+                        if (!resident) n = load_segment(srow, nvis, ch, k, a16);
+                        if (pass == 0) {
 #pragma unroll
-                        for (int j = 0; j < kKeysPerThread; ++j)
-                            if (j < n) atomicAdd(&hist[k[j] >> 21], 1u);
-                    } else {
+                            for (int j = 0; j < kKeysPerThread; ++j)
+                                if (j < n) atomicAdd(&h[k[j] >> 21], 1u);
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < kKeysPerThread; ++j)
-                            if (j < n && (k[j] & mask) == prefix) atomicAdd(&hist[(k[j] >> shift) & dmask], 1u);
+                            for (int j = 0; j < kKeysPerThread; ++j)
+                                if (j < n && (k[j] & mask) == prefix) atomicAdd(&h[(k[j] >> shift) & dmask], 1u);
+                        }
                     }
                 }
                 __syncthreads();
-                find_digit(hist, remaining, warp_tot, &s_digit, &s_remaining);
+                find_digit(h, remaining, warp_tot, &s_digit, &s_remaining, &s_count);
                 prefix |= s_digit << shift;
                 mask |= dmask << shift;
                 remaining = s_remaining;
+                clear_hist(h);  // read by nobody any more; the pass after next uses it
+                if (pass == 0 && resident && s_count <= (uint32_t)kCandCap) {
+                    // Gather the chosen bin's keys (any order: only counts matter).
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < kKeysPerThread; ++j) m |= (uint32_t)(j < n && (k[j] & mask) == prefix) << j;
+                    const uint32_t cnt = __popc(m);
+                    uint32_t incl = cnt;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if ((tid & 31) >= o) incl += y;
+                    }
+                    uint32_t wbase = 0;
+                    if ((tid & 31) == 31) wbase = atomicAdd(&s_ncand, incl);
+                    uint32_t at = __shfl_sync(0xffffffffu, wbase, 31) + incl - cnt;
+#pragma unroll
+                    for (int j = 0; j < kKeysPerThread; ++j)
+                        if ((m >> j) & 1u) cand[at++] = k[j];
+                    use_cand = true;
+                    __syncthreads();
+                }
             }
             const uint32_t T = prefix, need = remaining;  // keep every key > T and the first `need` keys == T
             // Place the chosen blocks in index order: one block-wide scan of the
@@ -494,7 +583,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
             uint32_t sel_run = 0, eq_run = 0;
             const bool vec4 = staged && p.c == 4;  // whole 16-byte stores into the staged row
             for (uint32_t ch = 0; ch < n_chunks; ++ch) {
-                if (!resident) n = load_segment(srow, nvis, ch, k);
+                if (!resident) n = load_segment(srow, nvis, ch, k, a16);
                 uint32_t gt_mask = 0, eq_mask = 0;  // bit j: key j of the segment
 #pragma unroll
                 for (int j = 0; j < kKeysPerThread; ++j) {
@@ -684,7 +773,7 @@ qsa_status launch_select(const qsa_route_problem *pr, const float *scores, const
     p.offset = (uint32_t)pr->query_position_offset;
     p.n_best = (uint32_t)(pr->token_budget / pr->compress_ratio);
     p.W = (uint32_t)(pr->token_budget + pr->compress_ratio - 1);
-    const size_t smem = p.W <= (uint32_t)kStageMax ? (size_t)p.W * sizeof(int32_t) : 0;
+    const size_t smem = select_smem_words(p.W) * sizeof(uint32_t);
     if (smem > 48 * 1024) {
         qsa_status st = cuda_status(
             cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
