@@ -371,40 +371,43 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t x, uint32_t *warp_tot, u
 
 // Given a digit histogram, finds the digit d holding the remaining-th largest
 // key (counting from the top bin), how many keys of bin d that rank needs, and
-// how many keys bin d holds.
-// Warp w owns kBinsPerWarp consecutive bins in best-first order; its lane l
-// reads bins 2047 - (kBinsPerWarp w + 32 j + l), so every read is
-// conflict-free, and warp scans give each bin's count of better keys.
-constexpr int kBinsPerWarp = kDigitBins / kSelWarps;
+// how many keys bin d holds.  In best-first order (position r = bin 2047 - r)
+// warp w owns positions 256 w .. 256 w + 255 and lane l eight consecutive ones,
+// i.e. the eight bins b0 .. b0 + 7 with b0 = 2040 - 256 w - 8 l, read as two
+// 16-byte words; one warp scan of the lanes' sums and the warps' totals give
+// every lane the count of better keys.
 __device__ __forceinline__ void find_digit(const uint32_t *hist, uint32_t remaining, uint32_t *warp_tot,
                                            uint32_t *s_digit, uint32_t *s_rem, uint32_t *s_cnt) {
+    static_assert(kDigitBins == 8 * kSelThreads, "eight bins per thread");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int J = kBinsPerWarp / 32;
-    uint32_t cnt[J], excl[J], run = 0;
+    const int b0 = kDigitBins - 8 - 256 * warp - 8 * lane;
+    const uint4 lo = reinterpret_cast<const uint4 *>(hist + b0)[0];
+    const uint4 hi = reinterpret_cast<const uint4 *>(hist + b0)[1];
+    const uint32_t cnt[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};  // bins b0 + 7 .. b0
+    uint32_t sum = 0;
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        cnt[j] = hist[kDigitBins - 1 - (kBinsPerWarp * warp + 32 * j + lane)];
-        uint32_t incl = cnt[j];
+    for (int q = 0; q < 8; ++q) sum += cnt[q];
+    uint32_t incl = sum;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        excl[j] = run + incl - cnt[j];
-        run += __shfl_sync(0xffffffffu, incl, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
     }
-    if (lane == 0) warp_tot[warp] = run;
+    if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
-    uint32_t base = 0;
+    uint32_t e = incl - sum;
 #pragma unroll
-    for (int w = 0; w < kSelWarps; ++w) base += w < warp ? warp_tot[w] : 0u;
+    for (int w = 0; w < kSelWarps; ++w) e += w < warp ? warp_tot[w] : 0u;
+    if (e < remaining && remaining <= e + sum) {
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const uint32_t e = base + excl[j];
-        if (e < remaining && remaining <= e + cnt[j]) {
-            *s_digit = (uint32_t)(kDigitBins - 1 - (kBinsPerWarp * warp + 32 * j + lane));
-            *s_rem = remaining - e;
-            *s_cnt = cnt[j];
+        for (int q = 0; q < 8; ++q) {
+            if (e + cnt[q] >= remaining) {
+                *s_digit = (uint32_t)(b0 + 7 - q);
+                *s_rem = remaining - e;
+                *s_cnt = cnt[q];
+                break;
+            }
+            e += cnt[q];
         }
     }
     __syncthreads();
@@ -499,10 +502,16 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
                 // Coalesced loads (a warp reads 32 consecutive scores), transposed
                 // through shared memory into each thread's contiguous segment; one
                 // pad word every 32 keys keeps both sides free of bank conflicts.
+                const float *src = srow + tid;
+                uint32_t *dst = region + tid + (tid >> 5);  // slot of key tid; key tid + 256 j is 264 j further
+                if (nvis == (uint32_t)kSelChunk) {
 #pragma unroll
-                for (int j = 0; j < kKeysPerThread; ++j) {
-                    const uint32_t i = (uint32_t)j * kSelThreads + tid;
-                    if (i < nvis) region[i + (i >> 5)] = score_key(load_once(srow + i));
+                    for (int j = 0; j < kKeysPerThread; ++j) dst[j * 264] = score_key(__ldg(src + j * kSelThreads));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kKeysPerThread; ++j)
+                        if ((uint32_t)j * kSelThreads + tid < nvis)
+                            dst[j * 264] = score_key(__ldg(src + j * kSelThreads));
                 }
                 __syncthreads();
                 const uint32_t i0 = (uint32_t)tid * kKeysPerThread;
