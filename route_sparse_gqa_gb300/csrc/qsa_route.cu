@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
     uint32_t *cand = region + 2 * kDigitBins;  // keys of the first pass's chosen bin
     int32_t *stage = reinterpret_cast<int32_t *>(region + 2 * kDigitBins + kCandCap);  // the output row
     __shared__ uint32_t warp_tot[kSelWarps];
-    __shared__ uint32_t s_digit, s_remaining, s_count, s_ncand;
+    __shared__ uint32_t s_digit, s_remaining, s_count;
     const int tid = threadIdx.x;
     const uint32_t t = blockIdx.x, b = blockIdx.y;
     const int64_t row = (int64_t)b * p.S_q + t;
@@ -528,9 +528,9 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
             // passes read only those.
             uint32_t prefix = 0, mask = 0, remaining = p.n_best;
             bool use_cand = false;
+            uint32_t c_mask = 0, g1_mask = 0, c_cnt = 0, c_at = 0, n_cand = 0;
             clear_hist(hist[0]);
             clear_hist(hist[1]);
-            if (tid == 0) s_ncand = 0;
             __syncthreads();
 #pragma unroll 1
             for (int pass = 0; pass < 3; ++pass) {
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
                 const uint32_t dmask = pass == 2 ? 0x3FFu : 0x7FFu;
                 uint32_t *h = hist[pass & 1];
                 if (use_cand) {
-                    for (uint32_t i = tid; i < s_ncand; i += kSelThreads) {
+                    for (uint32_t i = tid; i < n_cand; i += kSelThreads) {
                         const uint32_t kc = cand[i];
                         if ((kc & mask) == prefix) atomicAdd(&h[(kc >> shift) & dmask], 1u);
                     }
@@ -563,23 +563,24 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
                 remaining = s_remaining;
                 clear_hist(h);  // read by nobody any more; the pass after next uses it
                 if (pass == 0 && resident && s_count <= (uint32_t)kCandCap) {
-                    // Gather the chosen bin's keys (any order: only counts matter).
-                    uint32_t m = 0;
+                    // Gather the chosen bin's keys into shared memory in block order
+                    // (thread order = index order) and note, per thread, which keys
+                    // went there (c_mask) and which lie in better bins (g1_mask: all
+                    // of those are chosen).
 #pragma unroll
-                    for (int j = 0; j < kKeysPerThread; ++j) m |= (uint32_t)(j < n && (k[j] & mask) == prefix) << j;
-                    const uint32_t cnt = __popc(m);
-                    uint32_t incl = cnt;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if ((tid & 31) >= o) incl += y;
+                    for (int j = 0; j < kKeysPerThread; ++j) {
+                        const bool live = j < n;
+                        c_mask |= (uint32_t)(live && (k[j] & mask) == prefix) << j;
+                        g1_mask |= (uint32_t)(live && (k[j] >> 21) > s_digit) << j;
                     }
-                    uint32_t wbase = 0;
-                    if ((tid & 31) == 31) wbase = atomicAdd(&s_ncand, incl);
-                    uint32_t at = __shfl_sync(0xffffffffu, wbase, 31) + incl - cnt;
+                    c_cnt = __popc(c_mask);
+                    uint32_t total;
+                    c_at = block_scan(c_cnt, warp_tot, total);
+                    uint32_t at = c_at;
 #pragma unroll
                     for (int j = 0; j < kKeysPerThread; ++j)
-                        if ((m >> j) & 1u) cand[at++] = k[j];
+                        if ((c_mask >> j) & 1u) cand[at++] = k[j];
+                    n_cand = total;
                     use_cand = true;
                     __syncthreads();
                 }
@@ -594,10 +595,25 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
             for (uint32_t ch = 0; ch < n_chunks; ++ch) {
                 if (!resident) n = load_segment(srow, nvis, ch, k, a16);
                 uint32_t gt_mask = 0, eq_mask = 0;  // bit j: key j of the segment
+                if (use_cand) {
+                    // Keys in better bins than the first pass's are all > T; only this
+                    // thread's gathered keys (in order, one per set bit of c_mask) need
+                    // comparing.
+                    gt_mask = g1_mask;
+                    uint32_t mm = c_mask;
+                    for (uint32_t q = 0; q < c_cnt; ++q) {
+                        const uint32_t kc = cand[c_at + q];
+                        const uint32_t bit = mm & (0u - mm);
+                        mm ^= bit;
+                        if (kc > T) gt_mask |= bit;
+                        else if (kc == T) eq_mask |= bit;
+                    }
+                } else {
 #pragma unroll
-                for (int j = 0; j < kKeysPerThread; ++j) {
-                    gt_mask |= (uint32_t)(j < n && k[j] > T) << j;
-                    eq_mask |= (uint32_t)(j < n && k[j] == T) << j;
+                    for (int j = 0; j < kKeysPerThread; ++j) {
+                        gt_mask |= (uint32_t)(j < n && k[j] > T) << j;
+                        eq_mask |= (uint32_t)(j < n && k[j] == T) << j;
+                    }
                 }
                 const uint32_t eq = __popc(eq_mask);
                 uint32_t tot;
