@@ -343,6 +343,67 @@ def run_ours(args):
 LAUNCHES_PER_STEP = 7
 
 
+def pipelined_e2e(dev, host: dict, outs: dict, compute_fn, n: int, n_slots: int) -> float:
+    """Milliseconds per step of an end-to-end loop through the public API: every
+    step copies its own inputs (`host`, pinned) to the device and its results
+    (`compute_fn(device_inputs)` -> {name: tensor}) back into `outs` (pinned).
+
+    Pipelined like a training input pipeline: device inputs are in `n_slots`
+    buffers, the host->device copy of a later step runs on its own stream while a
+    step computes, and the device->host copy of a step's results on a third
+    stream.  Events order each buffer's reuse; all copies stay in the timed region."""
+    import torch
+
+    comp = torch.cuda.current_stream(dev)
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dev_in = [{name: torch.empty_like(t, device=dev) for name, t in host.items()} for _ in range(n_slots)]
+    copied = [torch.cuda.Event() for _ in range(n_slots)]   # inputs of a slot are on the device
+    used = [torch.cuda.Event() for _ in range(n_slots)]     # compute finished with a slot's inputs
+    drained = [None] * n_slots                              # results of a slot's last step are on the host
+
+    def copy_in(slot):
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(used[slot])
+            for name, t in host.items():
+                dev_in[slot][name].copy_(t, non_blocking=True)
+            copied[slot].record(h2d_s)
+
+    def compute(slot):
+        comp.wait_event(copied[slot])
+        res = compute_fn(dev_in[slot])
+        used[slot].record(comp)
+        done = torch.cuda.Event()
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(used[slot])
+            for name, t in res.items():
+                t.record_stream(d2h_s)
+                outs[name].copy_(t, non_blocking=True)
+            done.record(d2h_s)
+        drained[slot] = done
+
+    def run(k):
+        for i in range(min(n_slots - 1, k)):
+            copy_in(i % n_slots)
+        for i in range(k):
+            if i + n_slots - 1 < k:
+                copy_in((i + n_slots - 1) % n_slots)
+            compute(i % n_slots)
+        for e in drained:
+            if e is not None:
+                comp.wait_event(e)
+
+    run(2)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(comp)
+    h2d_s.wait_event(t0)
+    run(n)
+    t1.record(comp)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / n
+
+
 def run_e2e(case, w, dev, args, qsa, flop_step, world):
     import torch
 
@@ -361,64 +422,15 @@ def run_e2e(case, w, dev, args, qsa, flop_step, world):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
 
-    # Pipelined like a training input pipeline: device inputs are double-buffered, the host->device
-    # copy of step i+1 runs on its own stream while step i computes, and the device->host copy of
-    # step i's results on a third stream.  Every step still copies its own inputs in and its own
-    # results out inside the timed region; events order each buffer's reuse.
-    comp = torch.cuda.current_stream(dev)
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n_slots = int(os.environ.get("QSA_E2E_SLOTS", "2"))
-    dev_in = [{name: torch.empty_like(t, device=dev) for name, t in host.items()} for _ in range(n_slots)]
-    copied = [torch.cuda.Event() for _ in range(n_slots)]   # inputs of a slot are on the device
-    used = [torch.cuda.Event() for _ in range(n_slots)]     # compute finished with a slot's inputs
-    drained = [None] * n_slots                              # results of a slot's last step are on the host
-
-    def copy_in(slot):
-        with torch.cuda.stream(h2d_s):
-            h2d_s.wait_event(used[slot])
-            for name, t in host.items():
-                dev_in[slot][name].copy_(t, non_blocking=True)
-            copied[slot].record(h2d_s)
-
-    def compute(slot):
-        comp.wait_event(copied[slot])
-        x = dev_in[slot]
+    def compute_fn(x):
         plan = qsa.preprocess(x["q"], x["k"], x["v"], x["routes"], w.softmax_scale)
         o, lse = qsa.forward(plan, x["q"], x["k"], x["v"])
         dq, dk, dv = qsa.backward(plan, x["q"], x["k"], x["v"], o, lse, x["do"])
-        used[slot].record(comp)
-        res = (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))
-        done = torch.cuda.Event()
-        with torch.cuda.stream(d2h_s):
-            d2h_s.wait_event(used[slot])
-            for name, t in res:
-                t.record_stream(d2h_s)
-                outs[name].copy_(t, non_blocking=True)
-            done.record(d2h_s)
-        drained[slot] = done
+        return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
 
-    def run(n):
-        for i in range(min(n_slots - 1, n)):
-            copy_in(i % n_slots)
-        for i in range(n):
-            if i + n_slots - 1 < n:
-                copy_in((i + n_slots - 1) % n_slots)
-            compute(i % n_slots)
-        for e in drained:
-            if e is not None:
-                comp.wait_event(e)
-
-    run(2)
-    torch.cuda.synchronize()
+    n_slots = int(os.environ.get("QSA_E2E_SLOTS", "2"))
     n = max(3, args.steps // 2)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(comp)
-    h2d_s.wait_event(t0)
-    run(n)
-    t1.record(comp)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(t0.elapsed_time(t1) / n, dev)
+    ms = max_over_ranks(pipelined_e2e(dev, host, outs, compute_fn, n, n_slots), dev)
     return {"value": round(job_tflops(flop_step, world, ms), 3), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "pipeline": f"inputs in {n_slots} device buffers; later steps' H2D and earlier steps' D2H overlap each step's compute"}
@@ -586,37 +598,23 @@ def run_route_producer(args):
     _abi.check(lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream)))
 
     # End to end through the public binding with pinned host buffers: H2D of the
-    # index states and lengths, the producer, D2H of the route rows.
-    hq = bf(case.q).pin_memory()
-    hk = bf(case.k).pin_memory()
-    hl = torch.from_numpy(case.lengths).pin_memory()
-    hids = torch.empty((w.B, w.S_q, W_), dtype=torch.int32).pin_memory()
-    dq_, dk_, dl_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(lens)
+    # index states and lengths, the producer, D2H of the route rows (pipelined).
+    host = {"q": bf(case.q).pin_memory(), "k": bf(case.k).pin_memory(),
+            "lens": torch.from_numpy(case.lengths).pin_memory()}
+    outs = {"ids": torch.empty((w.B, w.S_q, W_), dtype=torch.int32).pin_memory()}
 
-    def e2e_step():
-        dq_.copy_(hq, non_blocking=True)
-        dk_.copy_(hk, non_blocking=True)
-        dl_.copy_(hl, non_blocking=True)
-        out = qsa.select_qsa_token_ids(dq_, dk_, dl_, w.budget, w.c, query_position_offset=w.offset,
-                                       global_sequence_length=w.S_global)
-        hids.copy_(out, non_blocking=True)
+    def compute_fn(x):
+        return {"ids": qsa.select_qsa_token_ids(x["q"], x["k"], x["lens"], w.budget, w.c,
+                                                query_position_offset=w.offset, global_sequence_length=w.S_global)}
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
+    n_slots = int(os.environ.get("QSA_E2E_SLOTS", "2"))
     n_e2e = max(3, min(args.steps, 10))
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(n_e2e):
-        e2e_step()
-    t1.record()
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / n_e2e, dev)
-    h2d = hq.numel() * 2 + hk.numel() * 2 + hl.numel() * 8
-    d2h = hids.numel() * 4
+    e2e_ms = max_over_ranks(pipelined_e2e(dev, host, outs, compute_fn, n_e2e, n_slots), dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
     e2e = {"value": round(job_tflops(flop, world, e2e_ms), 3), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-           "pipeline": "none: copies and compute in sequence on one stream"}
+           "pipeline": f"inputs in {n_slots} device buffers; later steps' H2D and earlier steps' D2H overlap each step's compute"}
 
     peaks, peak_src = load_peaks()
     hbm = float(peaks["hbm_gbs"])
