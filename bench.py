@@ -702,7 +702,7 @@ def run_route_cpu_baseline(case, w, flop, live_rows, args):
     import oracle
 
     oracle.build()
-    starts, rows, pairs = route_oracle_sample(case, w, args.route_rows)
+    starts, rows, pairs = route_oracle_sample(case, w, args.route_cpu_rows)
     secs = time_route_oracle(case, w, starts)
     return {"value": round(2 * w.H * w.D * pairs / secs / 1e12, 6), "unit": UNIT,
             "cores": min(oracle.omp_threads(), ROUTE_GROUP), "kind": "oracle", "seconds": round(secs, 2),
@@ -752,7 +752,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--route-producer", action="store_true",
                     help="measure the route producer (index scores + top-k selection) instead of the attention")
-    ap.add_argument("--route-rows", type=int, default=256, help="query rows in the route-producer oracle sample")
+    ap.add_argument("--route-rows", type=int, default=256,
+                    help="query rows per step of the route-producer reference (oracle) arm")
+    ap.add_argument("--route-cpu-rows", type=int, default=12288,
+                    help="query rows in the route-producer CPU-baseline oracle sample")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
