@@ -32,8 +32,11 @@
  * Conventions are those of qsa.h: device pointers unless named *_host, caller
  * owns all memory, work is queued on `stream` with no host synchronisation,
  * errors are returned (no fallback), qsa_last_error() explains the last one,
- * qsa_read_device_status(workspace) reports device-side failures, and index
- * arithmetic is 64-bit.
+ * and index arithmetic is 64-bit.  The workspace needs no initialisation:
+ * every call that scores clears its status word and work queue counters
+ * first; qsa_read_device_status(workspace) then reports (and clears) a
+ * device-side failure of that call, such as a bounded wait that gave up
+ * (QSA_ERR_TIMEOUT).  Calls sharing one workspace must be ordered.
  */
 #ifndef QSA_ROUTE_H_
 #define QSA_ROUTE_H_

@@ -758,6 +758,9 @@ qsa_status launch_scores(const qsa_route_problem *pr, const void *q, const void 
     p.sched = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kOffSched);
     p.status = reinterpret_cast<DeviceStatus *>(static_cast<char *>(ws) + kOffStatus);
     if (p.n_items > 2147483647LL) return route_fail(QSA_ERR_UNSUPPORTED, "too many query tiles");
+    // A fresh status word and work queue for this call (the workspace may be uninitialised memory).
+    qsa_status st = cuda_status(cudaMemsetAsync(ws, 0, kOffScores, stream), "cudaMemsetAsync");
+    if (st != QSA_OK) return st;
     const int64_t qd[4] = {p.D, p.H, p.S_q, p.B};
     const int64_t qs[3] = {pr->q_stride[2], pr->q_stride[1], pr->q_stride[0]};
     const uint32_t qbox[4] = {64, (uint32_t)p.H, (uint32_t)p.n_q, 1};
@@ -770,8 +773,6 @@ qsa_status launch_scores(const qsa_route_problem *pr, const void *q, const void 
     if (!tc_encode_bf16_map(&p.q_map, q, 4, qd, qs, qbox) || !tc_encode_bf16_map(&p.k_map, k, 3, kd, ks, kbox))
         return route_fail(QSA_ERR_UNSUPPORTED, "tensor map encoding failed for the index operands");
     const uint32_t smem = score_smem_bytes(p.D);
-    qsa_status st = cuda_status(cudaMemsetAsync(p.sched, 0, 2 * sizeof(int32_t), stream), "cudaMemsetAsync");
-    if (st != QSA_OK) return st;
     const int grid = (int)std::min<int64_t>(p.n_items, tc_num_sms());
     switch (p.H) {
         case 1: return launch_score_kernel<1>(p, grid, smem, stream);

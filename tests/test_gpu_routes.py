@@ -321,3 +321,48 @@ def test_full_size_train_step_sampled_rows():
 def test_cp_shard_sampled_rows():
     """Local rows at global offset 24576 against 8192 global blocks."""
     _sampled_rows_against_oracle(2, [0, 1, 8191])
+
+
+def test_forced_wait_timeout_in_the_score_kernel_is_reported():
+    """The score kernel bounds every pipeline wait; the host-side hook
+    QSA_DEBUG_WAIT_LIMIT_NS=0 makes them run out at once.  The call must report
+    QSA_ERR_TIMEOUT through the workspace status word, and the next normal call
+    in the same context must be right."""
+    import ctypes
+    import os
+
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+    from route_sparse_gqa_gb300 import _abi
+
+    case = W.make_index_case(0)
+    w = case.workload
+    dev = _dev()
+    q, k = bf16_to_device(case.q, dev), bf16_to_device(case.k, dev)
+    lens = torch.from_numpy(case.lengths).to(dev)
+    p, qq, kk = qsa.routes._problem(q, k, w.budget, w.c, w.offset, w.S_global)
+    lib = _abi.load()
+    n = lib.qsa_route_workspace_bytes(ctypes.byref(p))
+    ws = torch.full((n,), 0x5A, dtype=torch.uint8, device=dev)  # uninitialised-looking workspace
+    ids = torch.empty((w.B, w.S_q, w.budget + w.c - 1), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    os.environ["QSA_DEBUG_WAIT_LIMIT_NS"] = "0"
+    try:
+        _abi.check(lib.qsa_select_token_ids(ctypes.byref(p), qq.data_ptr(), kk.data_ptr(), lens.data_ptr(),
+                                            ws.data_ptr(), n, ids.data_ptr(), stream))
+    finally:
+        del os.environ["QSA_DEBUG_WAIT_LIMIT_NS"]
+    st = lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream))
+    assert st == 5, st  # QSA_ERR_TIMEOUT
+    assert lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream)) == 0
+    # A normal call afterwards, on the same workspace, is right.
+    _abi.check(lib.qsa_select_token_ids(ctypes.byref(p), qq.data_ptr(), kk.data_ptr(), lens.data_ptr(),
+                                        ws.data_ptr(), n, ids.data_ptr(), stream))
+    assert lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream)) == 0
+    torch.cuda.synchronize()
+    got = ids.cpu().numpy()
+    _row_structure(got, case.lengths, w.budget, w.c, w.offset, w.n_blocks)
+    qd, kd = f64(case.q), f64(case.k)
+    ref = oracle.index_scores(qd, kd, w.c, w.offset)
+    _assert_valid_topk(got, ref, _score_tol(qd, kd, ref), case.lengths, w.budget, w.c, w.offset)
