@@ -69,6 +69,7 @@ struct BwdParams {
     KVMaps kv[kMaxPairs];               // per (b, g): K/V row-gather and 64-row-run maps
     int64_t B, S_q, S_kv, Hq, Hkv, G, T, n_tiles, max_chunks;
     int64_t g0, n_g, n_items;
+    int32_t head_major;  // work queue order (qsa_queue.cuh)
     float sl2, scale;
     uint64_t wait_limit_ns;  // bound of every pipeline wait
     const int32_t *tile_nchunks;
@@ -541,6 +542,7 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
         const int64_t n_g = std::min<int64_t>(g_per_launch, a.Hkv - g0);
         p.g0 = g0;
         p.n_g = n_g;
+        p.head_major = tc_head_major_order(bw.f, n_g);
         p.n_items = n_g * a.B * t.n_tiles;
         for (int64_t b = 0; b < a.B; ++b)
             for (int64_t gi = 0; gi < n_g; ++gi)

@@ -83,7 +83,8 @@ struct FwdParams {
     const __nv_bfloat16 *q;
     int64_t qs0, qs1, qs2;
     int64_t B, S_q, Hq, G, T, n_tiles, max_chunks;
-    int64_t g0, n_g;   // KV heads handled by this launch
+    int64_t g0, n_g;     // KV heads handled by this launch
+    int32_t head_major;  // work queue order (qsa_queue.cuh)
     int64_t n_items;   // n_g * B * n_tiles
     float sl2;         // softmax_scale * log2(e)
     uint64_t wait_limit_ns;  // bound of every pipeline wait
@@ -597,6 +598,7 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
         const int64_t n_g = std::min<int64_t>(g_per_launch, a.Hkv - g0);
         p.g0 = g0;
         p.n_g = n_g;
+        p.head_major = tc_head_major_order(a, n_g);
         p.n_items = n_g * a.B * t.n_tiles;
         for (int64_t b = 0; b < a.B; ++b)
             for (int64_t gi = 0; gi < n_g; ++gi)

@@ -1,9 +1,15 @@
 // qsa_queue.cuh -- dynamic work queue of the tile kernels.
 //
 // An item is (KV head g, query tile).  Items are ranked heaviest first: rank r
-// is the r-th tile of the work order (tiles sorted by chunk count, descending)
-// paired with every KV head of the launch, so the queue index is
-// idx = r * n_g + (g - g0).  Each CTA's producer warp claims the next index with
+// is the r-th tile of the work order (tiles sorted by chunk count,
+// descending).  Two orders of (rank, head):
+//   interleaved  idx = r * n_g + (g - g0): every head's heaviest tiles first;
+//   head-major   idx = (g - g0) * (B * n_tiles) + r: head by head, heaviest
+//                first within a head.
+// Head-major keeps the K/V rows and fp32 dK/dV accumulators in use at any time
+// to about one head's, which stays in L2 for long sequences where all heads'
+// together would not; the launch chooses it when the heads' accumulators
+// together exceed L2 (otherwise interleaving balances the tail better).  Each CTA's producer warp claims the next index with
 // one atomic add on a global counter and publishes it in a small ring in shared
 // memory; the CTA's other roles take the items from the ring in the same order.
 // A CTA that finishes early therefore takes more items (list scheduling,
@@ -24,8 +30,15 @@ struct QueueItem {
 
 template <typename P>
 __device__ __forceinline__ void queue_decode(const P &p, int32_t idx, QueueItem &it) {
-    const int64_t rank = idx / p.n_g;
-    it.g = p.g0 + idx % p.n_g;
+    int64_t rank;
+    if (p.head_major) {
+        const int64_t per_head = p.B * p.n_tiles;
+        rank = idx % per_head;
+        it.g = p.g0 + idx / per_head;
+    } else {
+        rank = idx / p.n_g;
+        it.g = p.g0 + idx % p.n_g;
+    }
     it.tile = p.order[rank];
     it.b = it.tile / p.n_tiles;
     it.t = it.tile % p.n_tiles;

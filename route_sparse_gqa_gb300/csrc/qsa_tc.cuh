@@ -51,6 +51,11 @@ bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, 
 bool tc_encode_bf16_map(CUtensorMap *m, const void *base, int rank, const int64_t *dims, const int64_t *strides,
                         const uint32_t *box);
 
+// Work queue order of a tile-kernel launch over n_g KV heads: head by head when
+// those heads' fp32 dK/dV accumulators together exceed half of L2 (the K/V
+// rows and Q/dO tiles share the rest), else interleaved.
+bool tc_head_major_order(const AttnArgs &a, int64_t n_g);
+
 bool tc_forward_supported();
 bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t);
 cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s);

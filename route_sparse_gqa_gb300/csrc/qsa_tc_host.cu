@@ -87,6 +87,18 @@ bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, 
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool tc_head_major_order(const AttnArgs &a, int64_t n_g) {
+    static int64_t l2 = -1;
+    if (l2 < 0) {
+        int dev = 0, bytes = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&bytes, cudaDevAttrL2CacheSize, dev);
+        l2 = bytes > 0 ? bytes : (64ll << 20);
+    }
+    const int64_t acc_bytes = a.B * a.S_kv * n_g * kHeadDim * 2 * (int64_t)sizeof(float);
+    return acc_bytes > l2 / 2;
+}
+
 bool tc_encode_bf16_map(CUtensorMap *m, const void *base, int rank, const int64_t *dims, const int64_t *strides,
                         const uint32_t *box) {
     if (rank < 2 || rank > 5) return false;
