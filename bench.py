@@ -228,7 +228,7 @@ def run_ours(args):
         o, lse = qsa.forward(plan, q, k, v)
         if timers:
             timers[2].record()
-        dq, dk, dv = qsa.backward(plan, q, k, v, o, lse, do)
+        dq, dk, dv = qsa.backward(plan, q, k, v, o, lse, do, deterministic=args.deterministic)
         if timers:
             timers[3].record()
         return plan, o, lse, dq, dk, dv
@@ -318,7 +318,8 @@ def run_ours(args):
         "data": "synthetic",
         "config": {
             "workload": f"{w.name}: {w.summary}",
-            "step": "preprocess + forward + backward (fp32 dK/dV accumulation)",
+            "step": ("preprocess + forward + deterministic backward (fixed-point dK/dV sums)" if args.deterministic
+                     else "preprocess + forward + backward (fp32 dK/dV accumulation)"),
             "parallelism": f"replicas x{world}",
             "l2": "flushed before every timed step (256 MiB write outside the events)",
             "keff_total": wc["keff_total"],
@@ -425,7 +426,7 @@ def run_e2e(case, w, dev, args, qsa, flop_step, world):
     def compute_fn(x):
         plan = qsa.preprocess(x["q"], x["k"], x["v"], x["routes"], w.softmax_scale)
         o, lse = qsa.forward(plan, x["q"], x["k"], x["v"])
-        dq, dk, dv = qsa.backward(plan, x["q"], x["k"], x["v"], o, lse, x["do"])
+        dq, dk, dv = qsa.backward(plan, x["q"], x["k"], x["v"], o, lse, x["do"], deterministic=args.deterministic)
         return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
 
     n_slots = int(os.environ.get("QSA_E2E_SLOTS", "2"))
@@ -750,6 +751,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=6144, help="query rows in the CPU-baseline oracle sample")
     ap.add_argument("--ref-rows", type=int, default=160, help="query rows per step of the reference (oracle) arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time the bitwise reproducible backward (qsa_backward_deterministic)")
     ap.add_argument("--route-producer", action="store_true",
                     help="measure the route producer (index scores + top-k selection) instead of the attention")
     ap.add_argument("--route-rows", type=int, default=256,

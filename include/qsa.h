@@ -124,6 +124,22 @@ QSA_API qsa_status qsa_backward(const qsa_problem *problem, void *workspace, siz
                         const void *v, const void *o, const float *lse, const void *dout, void *dq, void *dk,
                         void *dv, float *dk_f32, float *dv_f32, cudaStream_t stream);
 
+/* The same backward with bitwise reproducible dK/dV (and dQ): no counterpart on
+ * the pages, whose FA4 backward has no deterministic mode (fa4_qsa
+ * fa4_sparse_gqa_attention).  Every dK/dV contribution x is accumulated as the
+ * 64-bit integer round(x * 2^32) with integer reductions, which are
+ * associative, so the sums do not depend on the order in which the GPU adds
+ * them; the sums are then converted to fp32 (dk_f32/dv_f32 when non-null) and
+ * BF16.  Resolution 2^-32 per contribution; contributions and sums must stay
+ * below 2^31 in magnitude.  dQ is accumulated in a fixed order in either call.
+ * Costs more than qsa_backward: 8 instead of 4 bytes of reduction traffic per
+ * contribution.  Arguments, layouts and errors are those of qsa_backward; the
+ * accumulators live in the workspace. */
+QSA_API qsa_status qsa_backward_deterministic(const qsa_problem *problem, void *workspace, size_t ws_bytes,
+                                              const void *q, const void *k, const void *v, const void *o,
+                                              const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                                              float *dk_f32, float *dv_f32, cudaStream_t stream);
+
 /* Copies the preprocessed routes out of the workspace (device to device, on
  * `stream`): ids [B,S_q,K] int32 = each row's valid IDs ascending and
  * deduplicated, then -1; counts [B,S_q] int32 = how many.  Either output may be

@@ -28,6 +28,7 @@ EXPORTS = (
     "qsa_preprocess",
     "qsa_forward",
     "qsa_backward",
+    "qsa_backward_deterministic",
     "qsa_copy_route_sets",
     "qsa_forward_no_alloc",
     "qsa_read_device_status",
@@ -90,6 +91,7 @@ def load() -> ctypes.CDLL:
         lib.qsa_preprocess.argtypes = [P, vp, vp, sz, vp]
         lib.qsa_forward.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp]
         lib.qsa_backward.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.qsa_backward_deterministic.argtypes = [P, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_copy_route_sets.argtypes = [P, vp, sz, vp, vp, vp]
         lib.qsa_forward_no_alloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_read_device_status.argtypes = [vp, vp]
@@ -106,7 +108,8 @@ def load() -> ctypes.CDLL:
         lib.qsa_index_scores.argtypes = [R, vp, vp, vp, vp, sz, vp, vp]
         lib.qsa_select_from_scores.argtypes = [R, vp, vp, vp, sz, vp, vp]
         lib.qsa_select_token_ids.argtypes = [R, vp, vp, vp, vp, sz, vp, vp]
-        for name in ("qsa_check_problem", "qsa_preprocess", "qsa_forward", "qsa_backward", "qsa_copy_route_sets",
+        for name in ("qsa_check_problem", "qsa_preprocess", "qsa_forward", "qsa_backward",
+                     "qsa_backward_deterministic", "qsa_copy_route_sets",
                      "qsa_forward_no_alloc", "qsa_read_device_status", "qsa_route_check_problem",
                      "qsa_index_scores", "qsa_select_from_scores", "qsa_select_token_ids"):
             getattr(lib, name).restype = ctypes.c_int

@@ -133,8 +133,12 @@ def forward(plan: RoutePlan, query, key, value):
     return o, lse
 
 
-def backward(plan: RoutePlan, query, key, value, out, lse, grad_out, fp32_dkdv: bool = False):
-    """Returns (dQ, dK, dV) in bf16, plus the fp32 dK/dV sums when fp32_dkdv."""
+def backward(plan: RoutePlan, query, key, value, out, lse, grad_out, fp32_dkdv: bool = False,
+             deterministic: bool = False):
+    """Returns (dQ, dK, dV) in bf16, plus the fp32 dK/dV sums when fp32_dkdv.
+
+    ``deterministic`` selects the bitwise reproducible backward (dK/dV summed as
+    fixed-point integers, ``qsa_backward_deterministic``)."""
     p = plan.problem
     query, key, value = _attn_operand(query), _attn_operand(key), _attn_operand(value)
     pp = make_problem(query, key, value, _RouteShape(p), p.softmax_scale)
@@ -149,7 +153,9 @@ def backward(plan: RoutePlan, query, key, value, out, lse, grad_out, fp32_dkdv: 
     if fp32_dkdv:
         dk32 = torch.empty((p.B, p.S_kv, p.Hkv, p.D), dtype=torch.float32, device=dev)
         dv32 = torch.empty_like(dk32)
-    _abi.check(_abi.load().qsa_backward(
+    lib = _abi.load()
+    entry = lib.qsa_backward_deterministic if deterministic else lib.qsa_backward
+    _abi.check(entry(
         pp, plan.workspace.data_ptr(), plan.nbytes, query.data_ptr(), key.data_ptr(), value.data_ptr(),
         out.data_ptr(), lse.data_ptr(), grad_out.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
         dk32.data_ptr() if dk32 is not None else None, dv32.data_ptr() if dv32 is not None else None,
@@ -173,24 +179,26 @@ class _RouteShape:
 
 class _QSAFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, query, key, value, routes, softmax_scale):
+    def forward(ctx, query, key, value, routes, softmax_scale, deterministic):
         plan = preprocess(query, key, value, routes, softmax_scale)
         o, lse = forward(plan, query, key, value)
         ctx.save_for_backward(query, key, value, o, lse)
         ctx.plan = plan
+        ctx.deterministic = deterministic
         return o
 
     @staticmethod
     def backward(ctx, grad_out):
         query, key, value, o, lse = ctx.saved_tensors
-        dq, dk, dv = backward(ctx.plan, query, key, value, o, lse, grad_out)
-        return dq, dk, dv, None, None
+        dq, dk, dv = backward(ctx.plan, query, key, value, o, lse, grad_out, deterministic=ctx.deterministic)
+        return dq, dk, dv, None, None, None
 
 
-def qsa_attention(query, key, value, selected_token_ids, softmax_scale=None):
+def qsa_attention(query, key, value, selected_token_ids, softmax_scale=None, deterministic: bool = False):
     """Exact route-set sparse GQA attention; differentiable in query/key/value
-    (first order).  Returns BF16 ``[B,S_q,Hq,D]``."""
-    return _QSAFunction.apply(query, key, value, selected_token_ids, softmax_scale)
+    (first order).  Returns BF16 ``[B,S_q,Hq,D]``.  ``deterministic`` makes the
+    backward bitwise reproducible."""
+    return _QSAFunction.apply(query, key, value, selected_token_ids, softmax_scale, deterministic)
 
 
 def qsa_attention_with_lse(query, key, value, selected_token_ids, softmax_scale=None):

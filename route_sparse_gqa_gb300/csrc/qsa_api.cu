@@ -88,11 +88,12 @@ Layout make_layout(const qsa_problem *p) {
     off = align256(off + tiles * sizeof(int32_t));
     L.off_delta = off;
     off = align256(off + p->B * p->Hq * p->S_q * sizeof(float));
-    const size_t kv_f32 = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * sizeof(float);
+    // dK/dV accumulators: fp32, or 64-bit fixed point for the deterministic backward.
+    const size_t kv_acc = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * sizeof(unsigned long long);
     L.off_dk = off;
-    off = align256(off + kv_f32);
+    off = align256(off + kv_acc);
     L.off_dv = off;
-    off = align256(off + kv_f32);
+    off = align256(off + kv_acc);
     L.total = off;
     return L;
 }
@@ -174,6 +175,95 @@ TileArgs tile_args(const qsa_problem *p, const Layout &L, void *ws) {
 
 qsa_status report_error(qsa_status st, const char *msg) { return fail(st, "%s", msg); }
 
+}  // namespace qsa
+
+namespace qsa {
+namespace {
+qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const void *q, const void *k, const void *v,
+                         const void *o, const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                         float *dk_f32, float *dv_f32, bool deterministic, cudaStream_t stream) {
+    Layout L;
+    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    if (st != QSA_OK) return st;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+        return fail(QSA_ERR_INVALID_ARGUMENT, "null tensor pointer");
+    if ((dk_f32 == nullptr) != (dv_f32 == nullptr))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "dk_f32 and dv_f32 must both be given or both be null");
+    const void *al[] = {q, k, v, o, dout, dq, dk, dv};
+    for (const void *x : al)
+        if (!aligned16(x)) return fail(QSA_ERR_UNSUPPORTED, "bf16 tensors must be 16-byte aligned");
+    if ((dk_f32 && !aligned16(dk_f32)) || (dv_f32 && !aligned16(dv_f32)))
+        return fail(QSA_ERR_UNSUPPORTED, "fp32 accumulators must be 16-byte aligned");
+    uintptr_t q0, q1, k0, k1, v0, v1;
+    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, q0, q1);
+    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, k0, k1);
+    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, v0, v1);
+    const size_t nq = 2 * (size_t)(p->B * p->S_q * p->Hq * kHeadDim);
+    const size_t nkv = 2 * (size_t)(p->B * p->S_kv * p->Hkv * kHeadDim);
+    auto u = [](const void *x) { return reinterpret_cast<uintptr_t>(x); };
+    const uintptr_t ins[6][2] = {{q0, q1}, {k0, k1}, {v0, v1}, {u(o), u(o) + nq}, {u(dout), u(dout) + nq},
+                                 {u(lse), u(lse) + 4 * (size_t)(p->B * p->Hq * p->S_q)}};
+    uintptr_t outs[5][2] = {{u(dq), u(dq) + nq}, {u(dk), u(dk) + nkv}, {u(dv), u(dv) + nkv}, {0, 0}, {0, 0}};
+    int nout = 3;
+    if (dk_f32) {
+        outs[3][0] = u(dk_f32);
+        outs[3][1] = u(dk_f32) + 2 * nkv;
+        outs[4][0] = u(dv_f32);
+        outs[4][1] = u(dv_f32) + 2 * nkv;
+        nout = 5;
+    }
+    const uintptr_t w0 = u(ws), w1 = w0 + L.total;
+    for (int i = 0; i < nout; ++i) {
+        for (auto &r : ins)
+            if (overlaps(outs[i][0], outs[i][1], r[0], r[1]))
+                return fail(QSA_ERR_INVALID_ARGUMENT, "a gradient output overlaps an input");
+        if (overlaps(outs[i][0], outs[i][1], w0, w1))
+            return fail(QSA_ERR_INVALID_ARGUMENT, "a gradient output overlaps the workspace");
+        for (int j = 0; j < i; ++j)
+            if (overlaps(outs[i][0], outs[i][1], outs[j][0], outs[j][1]))
+                return fail(QSA_ERR_INVALID_ARGUMENT, "gradient outputs overlap each other");
+    }
+    BwdArgs b{};
+    b.f = attn_args(p, L, ws, q, k, v);
+    b.o = static_cast<const __nv_bfloat16 *>(o);
+    b.dout = static_cast<const __nv_bfloat16 *>(dout);
+    b.lse = lse;
+    b.delta = at<float>(ws, L.off_delta);
+    b.dq = static_cast<__nv_bfloat16 *>(dq);
+    b.dk = static_cast<__nv_bfloat16 *>(dk);
+    b.dv = static_cast<__nv_bfloat16 *>(dv);
+    const size_t n_kv = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim;
+    cudaError_t e;
+    if (deterministic) {
+        // Fixed-point accumulators in the workspace; the caller's fp32 buffers (if any) receive the sums.
+        b.dk_fx = at<unsigned long long>(ws, L.off_dk);
+        b.dv_fx = at<unsigned long long>(ws, L.off_dv);
+        b.dk_acc = dk_f32;
+        b.dv_acc = dv_f32;
+        e = cudaMemsetAsync(b.dk_fx, 0, n_kv * sizeof(unsigned long long), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(b.dv_fx, 0, n_kv * sizeof(unsigned long long), stream);
+    } else {
+        b.dk_acc = dk_f32 ? dk_f32 : at<float>(ws, L.off_dk);
+        b.dv_acc = dv_f32 ? dv_f32 : at<float>(ws, L.off_dv);
+        e = cudaMemsetAsync(b.dk_acc, 0, n_kv * sizeof(float), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(b.dv_acc, 0, n_kv * sizeof(float), stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the dK/dV accumulators");
+    e = launch_delta(b, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "delta launch");
+    const TileArgs ta = tile_args(p, L, ws);
+    if (L.T && tc_backward_supported() && tc_backward_shape_ok(b.f, ta)) {
+        e = launch_tc_backward(b, ta, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
+    } else {
+        e = launch_rowwise_backward(b, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "rowwise backward launch");
+    }
+    e = launch_convert_dkdv(b, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dK/dV conversion launch");
+    return QSA_OK;
+}
+}  // namespace
 }  // namespace qsa
 
 using namespace qsa;
@@ -269,75 +359,13 @@ qsa_status qsa_forward(const qsa_problem *p, void *ws, size_t ws_bytes, const vo
 qsa_status qsa_backward(const qsa_problem *p, void *ws, size_t ws_bytes, const void *q, const void *k, const void *v,
                         const void *o, const float *lse, const void *dout, void *dq, void *dk, void *dv,
                         float *dk_f32, float *dv_f32, cudaStream_t stream) {
-    Layout L;
-    qsa_status st = check_ws(p, ws, ws_bytes, L);
-    if (st != QSA_OK) return st;
-    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
-        return fail(QSA_ERR_INVALID_ARGUMENT, "null tensor pointer");
-    if ((dk_f32 == nullptr) != (dv_f32 == nullptr))
-        return fail(QSA_ERR_INVALID_ARGUMENT, "dk_f32 and dv_f32 must both be given or both be null");
-    const void *al[] = {q, k, v, o, dout, dq, dk, dv};
-    for (const void *x : al)
-        if (!aligned16(x)) return fail(QSA_ERR_UNSUPPORTED, "bf16 tensors must be 16-byte aligned");
-    if ((dk_f32 && !aligned16(dk_f32)) || (dv_f32 && !aligned16(dv_f32)))
-        return fail(QSA_ERR_UNSUPPORTED, "fp32 accumulators must be 16-byte aligned");
-    uintptr_t q0, q1, k0, k1, v0, v1;
-    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, q0, q1);
-    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, k0, k1);
-    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, v0, v1);
-    const size_t nq = 2 * (size_t)(p->B * p->S_q * p->Hq * kHeadDim);
-    const size_t nkv = 2 * (size_t)(p->B * p->S_kv * p->Hkv * kHeadDim);
-    auto u = [](const void *x) { return reinterpret_cast<uintptr_t>(x); };
-    const uintptr_t ins[6][2] = {{q0, q1}, {k0, k1}, {v0, v1}, {u(o), u(o) + nq}, {u(dout), u(dout) + nq},
-                                 {u(lse), u(lse) + 4 * (size_t)(p->B * p->Hq * p->S_q)}};
-    uintptr_t outs[5][2] = {{u(dq), u(dq) + nq}, {u(dk), u(dk) + nkv}, {u(dv), u(dv) + nkv}, {0, 0}, {0, 0}};
-    int nout = 3;
-    if (dk_f32) {
-        outs[3][0] = u(dk_f32);
-        outs[3][1] = u(dk_f32) + 2 * nkv;
-        outs[4][0] = u(dv_f32);
-        outs[4][1] = u(dv_f32) + 2 * nkv;
-        nout = 5;
-    }
-    const uintptr_t w0 = u(ws), w1 = w0 + L.total;
-    for (int i = 0; i < nout; ++i) {
-        for (auto &r : ins)
-            if (overlaps(outs[i][0], outs[i][1], r[0], r[1]))
-                return fail(QSA_ERR_INVALID_ARGUMENT, "a gradient output overlaps an input");
-        if (overlaps(outs[i][0], outs[i][1], w0, w1))
-            return fail(QSA_ERR_INVALID_ARGUMENT, "a gradient output overlaps the workspace");
-        for (int j = 0; j < i; ++j)
-            if (overlaps(outs[i][0], outs[i][1], outs[j][0], outs[j][1]))
-                return fail(QSA_ERR_INVALID_ARGUMENT, "gradient outputs overlap each other");
-    }
-    BwdArgs b{};
-    b.f = attn_args(p, L, ws, q, k, v);
-    b.o = static_cast<const __nv_bfloat16 *>(o);
-    b.dout = static_cast<const __nv_bfloat16 *>(dout);
-    b.lse = lse;
-    b.delta = at<float>(ws, L.off_delta);
-    b.dq = static_cast<__nv_bfloat16 *>(dq);
-    b.dk = static_cast<__nv_bfloat16 *>(dk);
-    b.dv = static_cast<__nv_bfloat16 *>(dv);
-    b.dk_acc = dk_f32 ? dk_f32 : at<float>(ws, L.off_dk);
-    b.dv_acc = dv_f32 ? dv_f32 : at<float>(ws, L.off_dv);
-    const size_t kv_f32 = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * sizeof(float);
-    cudaError_t e = cudaMemsetAsync(b.dk_acc, 0, kv_f32, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(b.dv_acc, 0, kv_f32, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the dK/dV accumulators");
-    e = launch_delta(b, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "delta launch");
-    const TileArgs ta = tile_args(p, L, ws);
-    if (L.T && tc_backward_supported() && tc_backward_shape_ok(b.f, ta)) {
-        e = launch_tc_backward(b, ta, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
-    } else {
-        e = launch_rowwise_backward(b, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "rowwise backward launch");
-    }
-    e = launch_convert_dkdv(b, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "dK/dV conversion launch");
-    return QSA_OK;
+    return backward_impl(p, ws, ws_bytes, q, k, v, o, lse, dout, dq, dk, dv, dk_f32, dv_f32, false, stream);
+}
+
+qsa_status qsa_backward_deterministic(const qsa_problem *p, void *ws, size_t ws_bytes, const void *q, const void *k,
+                                      const void *v, const void *o, const float *lse, const void *dout, void *dq,
+                                      void *dk, void *dv, float *dk_f32, float *dv_f32, cudaStream_t stream) {
+    return backward_impl(p, ws, ws_bytes, q, k, v, o, lse, dout, dq, dk, dv, dk_f32, dv_f32, true, stream);
 }
 
 qsa_status qsa_copy_route_sets(const qsa_problem *p, const void *ws, size_t ws_bytes, int32_t *ids, int32_t *counts,

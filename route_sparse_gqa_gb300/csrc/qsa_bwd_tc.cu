@@ -80,6 +80,7 @@ struct BwdParams {
     const float *lse, *delta;
     __nv_bfloat16 *dq;
     float *dk_acc, *dv_acc;
+    unsigned long long *dk_fx, *dv_fx;  // deterministic mode: fixed-point accumulators
     DeviceStatus *status;
 };
 
@@ -92,6 +93,8 @@ enum BarId {
     kDQReady, kDQFree, kDrain, kSFull
 };
 
+// kDet: the flush adds dK/dV as fixed-point integers (order-independent, bitwise reproducible sums).
+template <bool kDet>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -446,8 +449,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             queue_decode(p, idx, it);
             if (it.nch == 0) continue;
             const int64_t row_stride = p.Hkv * kHeadDim;
-            float *dk_base = p.dk_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
-            float *dv_base = p.dv_acc + (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
+            const int64_t base_off = (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
+            float *dk_base = kDet ? nullptr : p.dk_acc + base_off;
+            float *dv_base = kDet ? nullptr : p.dv_acc + base_off;
+            unsigned long long *dk_fx_base = kDet ? p.dk_fx + base_off : nullptr;
+            unsigned long long *dv_fx_base = kDet ? p.dv_fx + base_off : nullptr;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 // The chunk's 64 keys, one pair per lane, broadcast below with shuffles.  The loop has no
                 // branch: a partial chunk's padding columns have empty membership, so their dK^T/dV^T
@@ -474,8 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     for (int j = 0; j < 64; ++j) {
                         const int32_t key = __shfl_sync(0xffffffffu, j < 32 ? key_lo : key_hi, j & 31);
                         const int64_t off = (int64_t)key * row_stride + h * 128;
-                        red_add_f32(dk_base + off, __uint_as_float(a[j >> 5][j & 31]));
-                        red_add_f32(dv_base + off, __uint_as_float(v[j >> 5][j & 31]));
+                        if (kDet) {
+                            red_add_fx(dk_fx_base + off, __uint_as_float(a[j >> 5][j & 31]));
+                            red_add_fx(dv_fx_base + off, __uint_as_float(v[j >> 5][j & 31]));
+                        } else {
+                            red_add_f32(dk_base + off, __uint_as_float(a[j >> 5][j & 31]));
+                            red_add_f32(dv_base + off, __uint_as_float(v[j >> 5][j & 31]));
+                        }
                     }
                 }
                 if (!ok) break;
@@ -509,7 +520,10 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
         return cudaErrorInvalidValue;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -537,6 +551,8 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
     p.dq = bw.dq;
     p.dk_acc = bw.dk_acc;
     p.dv_acc = bw.dv_acc;
+    p.dk_fx = bw.dk_fx;
+    p.dv_fx = bw.dv_fx;
     p.status = a.status;
     for (int64_t g0 = 0; g0 < a.Hkv; g0 += g_per_launch) {
         const int64_t n_g = std::min<int64_t>(g_per_launch, a.Hkv - g0);
@@ -548,7 +564,10 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
             for (int64_t gi = 0; gi < n_g; ++gi)
                 if (!tc_encode_kv_maps(&p.kv[b * n_g + gi], a, b, g0 + gi)) return cudaErrorInvalidValue;
         const int grid = (int)std::min<int64_t>(p.n_items, sms);
-        tc_bwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+        if (bw.dk_fx)
+            tc_bwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
+        else
+            tc_bwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

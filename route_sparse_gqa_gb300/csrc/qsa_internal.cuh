@@ -29,7 +29,7 @@ struct Layout {
     int64_t n_tiles;     // query tiles per batch row
     int64_t max_chunks;  // capacity of one tile's chunk list
     size_t off_status, off_sched, off_counts, off_ids, off_tile_nchunks, off_tile_keys, off_tile_masks, off_order;
-    size_t off_delta, off_dk, off_dv, total;
+    size_t off_delta, off_dk, off_dv, total;  // off_dk/off_dv: 8 bytes per element (fp32 or fixed point)
 };
 
 // Device-side failure sites (DeviceStatus::where).
@@ -120,10 +120,30 @@ struct BwdArgs {
     const float *lse;
     float *delta;  // [B, Hq, S_q]
     __nv_bfloat16 *dq, *dk, *dv;
-    float *dk_acc, *dv_acc;  // fp32 [B, S_kv, Hkv, D]
+    float *dk_acc, *dv_acc;  // fp32 [B, S_kv, Hkv, D]: the accumulators, or (deterministic) fp32 outputs / null
+    // Deterministic mode: fixed-point accumulators [B, S_kv, Hkv, D], else null.
+    unsigned long long *dk_fx, *dv_fx;
 };
-cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s);
+
+// Deterministic dK/dV: every contribution x is added as the integer round(x * 2^32)
+// with a 64-bit integer reduction.  Integer addition is associative, so the sum
+// does not depend on the order in which the contributions arrive, and the result
+// is bitwise reproducible.  Resolution 2^-32 per contribution; the two's
+// complement sums are exact as long as each contribution and the final sum stay
+// below 2^31 in magnitude (intermediate wrap-around cancels).
+constexpr float kFxScale = 4294967296.0f;       // 2^32
+constexpr double kFxInvScale = 1.0 / 4294967296.0;
+
+__device__ __forceinline__ void red_add_fx(unsigned long long *addr, float x) {
+    const long long v = __float2ll_rn(x * kFxScale);
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ float fx_to_f32(unsigned long long v) {
+    return (float)((double)(long long)v * kFxInvScale);
+}
+cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s);  // deterministic when a.dk_fx is set
 cudaError_t launch_delta(const BwdArgs &a, cudaStream_t s);
-cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s);
+cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s);  // from a.dk_fx when set
 
 }  // namespace qsa

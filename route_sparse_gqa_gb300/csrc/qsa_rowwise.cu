@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(BwdArgs a) {
     }
 }
 
+// kDet: dK/dV contributions go to the fixed-point accumulators (order-independent sums).
+template <bool kDet>
 __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
     const AttnArgs &f = a.f;
     const int64_t row = blockIdx.x, g = blockIdx.y;
@@ -127,8 +129,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
     const float sl2 = f.scale * kLog2e;
     const __nv_bfloat16 *kbase = f.k + b * f.ks0 + g * f.ks2 + lane * 8;
     const __nv_bfloat16 *vbase = f.v + b * f.vs0 + g * f.vs2 + lane * 8;
-    float *dkbase = a.dk_acc + (b * f.S_kv * f.Hkv + g) * kHeadDim + lane * 8;
-    float *dvbase = a.dv_acc + (b * f.S_kv * f.Hkv + g) * kHeadDim + lane * 8;
+    float *dkbase = kDet ? nullptr : a.dk_acc + (b * f.S_kv * f.Hkv + g) * kHeadDim + lane * 8;
+    float *dvbase = kDet ? nullptr : a.dv_acc + (b * f.S_kv * f.Hkv + g) * kHeadDim + lane * 8;
     for (int64_t hl = warp; hl < f.G; hl += kWarps) {
         const int64_t h = g * f.G + hl;
         float qf[8], df[8], dq[8];
@@ -181,12 +183,21 @@ __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) dq[i] = fmaf(ds, kf[u][i], dq[i]);
                 const float c = f.scale * ds;
-                float *dkj = dkbase + j[u] * f.Hkv * kHeadDim;
-                float *dvj = dvbase + j[u] * f.Hkv * kHeadDim;
-                red_add_v4(dkj, c * qf[0], c * qf[1], c * qf[2], c * qf[3]);
-                red_add_v4(dkj + 4, c * qf[4], c * qf[5], c * qf[6], c * qf[7]);
-                red_add_v4(dvj, p * df[0], p * df[1], p * df[2], p * df[3]);
-                red_add_v4(dvj + 4, p * df[4], p * df[5], p * df[6], p * df[7]);
+                if (kDet) {
+                    const int64_t e0 = ((b * f.S_kv + j[u]) * f.Hkv + g) * kHeadDim + lane * 8;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        red_add_fx(a.dk_fx + e0 + i, c * qf[i]);
+                        red_add_fx(a.dv_fx + e0 + i, p * df[i]);
+                    }
+                } else {
+                    float *dkj = dkbase + j[u] * f.Hkv * kHeadDim;
+                    float *dvj = dvbase + j[u] * f.Hkv * kHeadDim;
+                    red_add_v4(dkj, c * qf[0], c * qf[1], c * qf[2], c * qf[3]);
+                    red_add_v4(dkj + 4, c * qf[4], c * qf[5], c * qf[6], c * qf[7]);
+                    red_add_v4(dvj, p * df[0], p * df[1], p * df[2], p * df[3]);
+                    red_add_v4(dvj + 4, p * df[4], p * df[5], p * df[6], p * df[7]);
+                }
             }
         }
 #pragma unroll
@@ -207,6 +218,29 @@ __global__ void convert_kernel(const float *dk, const float *dv, __nv_bfloat16 *
     }
 }
 
+// Fixed-point sums -> bf16 gradients, and fp32 copies when dk32/dv32 are given.
+__global__ void convert_fx_kernel(const unsigned long long *dk, const unsigned long long *dv, __nv_bfloat16 *dkb,
+                                  __nv_bfloat16 *dvb, float *dk32, float *dv32, int64_t n8) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
+        float kf[8], vf[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            kf[e] = fx_to_f32(dk[8 * i + e]);
+            vf[e] = fx_to_f32(dv[8 * i + e]);
+        }
+        reinterpret_cast<uint4 *>(dkb)[i] = f32x8_to_bf16(kf);
+        reinterpret_cast<uint4 *>(dvb)[i] = f32x8_to_bf16(vf);
+        if (dk32) {
+            float4 *k4 = reinterpret_cast<float4 *>(dk32) + 2 * i;
+            float4 *v4 = reinterpret_cast<float4 *>(dv32) + 2 * i;
+            k4[0] = make_float4(kf[0], kf[1], kf[2], kf[3]);
+            k4[1] = make_float4(kf[4], kf[5], kf[6], kf[7]);
+            v4[0] = make_float4(vf[0], vf[1], vf[2], vf[3]);
+            v4[1] = make_float4(vf[4], vf[5], vf[6], vf[7]);
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_rowwise_forward(const AttnArgs &a, __nv_bfloat16 *o, float *lse, cudaStream_t s) {
@@ -222,7 +256,10 @@ cudaError_t launch_delta(const BwdArgs &a, cudaStream_t s) {
 
 cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s) {
     dim3 grid((unsigned)(a.f.B * a.f.S_q), (unsigned)a.f.Hkv);
-    rowwise_bwd_kernel<<<grid, kThreads, 0, s>>>(a);
+    if (a.dk_fx)
+        rowwise_bwd_kernel<true><<<grid, kThreads, 0, s>>>(a);
+    else
+        rowwise_bwd_kernel<false><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -230,7 +267,10 @@ cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s) {
     const int64_t n8 = a.f.B * a.f.S_kv * a.f.Hkv * kHeadDim / 8;
     int64_t nb = (n8 + 255) / 256;
     int blocks = (int)(nb < 152 * 16 ? nb : 152 * 16);
-    convert_kernel<<<blocks, 256, 0, s>>>(a.dk_acc, a.dv_acc, a.dk, a.dv, n8);
+    if (a.dk_fx)
+        convert_fx_kernel<<<blocks, 256, 0, s>>>(a.dk_fx, a.dv_fx, a.dk, a.dv, a.dk_acc, a.dv_acc, n8);
+    else
+        convert_kernel<<<blocks, 256, 0, s>>>(a.dk_acc, a.dv_acc, a.dk, a.dv, n8);
     return cudaGetLastError();
 }
 

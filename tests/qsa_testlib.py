@@ -24,7 +24,7 @@ def f64(bits: np.ndarray) -> np.ndarray:
 
 
 def run_library(case_q, case_k, case_v, case_do, routes_np, scale, device="cuda:0", fp32_dkdv=False,
-                transform=None):
+                transform=None, deterministic=False):
     """Runs preprocess, forward and backward; returns numpy outputs (float64 /
     int32) and the plan.  ``transform`` may rewrap the device tensors (to test
     strided inputs)."""
@@ -39,7 +39,7 @@ def run_library(case_q, case_k, case_v, case_do, routes_np, scale, device="cuda:
         q, k, v, routes = transform(q, k, v, routes)
     plan = qsa.preprocess(q, k, v, routes, scale)
     o, lse = qsa.forward(plan, q, k, v)
-    res = qsa.backward(plan, q, k, v, o, lse, do, fp32_dkdv=fp32_dkdv)
+    res = qsa.backward(plan, q, k, v, o, lse, do, fp32_dkdv=fp32_dkdv, deterministic=deterministic)
     ids, counts = plan.route_sets()
     plan.device_status()
     torch.cuda.synchronize()
