@@ -126,15 +126,16 @@ QSA_API qsa_status qsa_backward(const qsa_problem *problem, void *workspace, siz
 
 /* The same backward with bitwise reproducible dK/dV (and dQ): no counterpart on
  * the pages, whose FA4 backward has no deterministic mode (fa4_qsa
- * fa4_sparse_gqa_attention).  Every dK/dV contribution x is accumulated as the
- * 64-bit integer round(x * 2^32) with integer reductions, which are
- * associative, so the sums do not depend on the order in which the GPU adds
- * them; the sums are then converted to fp32 (dk_f32/dv_f32 when non-null) and
- * BF16.  Resolution 2^-32 per contribution; contributions and sums must stay
- * below 2^31 in magnitude.  dQ is accumulated in a fixed order in either call.
- * Costs more than qsa_backward: 8 instead of 4 bytes of reduction traffic per
- * contribution.  Arguments, layouts and errors are those of qsa_backward; the
- * accumulators live in the workspace. */
+ * fa4_sparse_gqa_attention).  Every dK/dV contribution x is rounded once to the
+ * integer round(x * 2^24); the GPU sums those integers modulo 2^32 (integer
+ * addition: exact in any order) next to an ordinary fp32 sum of x, and the exact
+ * sum is recovered as the value congruent to the integer sum modulo 2^32 that
+ * is nearest to the fp32 estimate (which stays far closer than the 2^7 that
+ * requires).  The results depend on the inputs only; they are converted to fp32
+ * (dk_f32/dv_f32 when non-null) and BF16.  Resolution 2^-24 per contribution.
+ * dQ is accumulated in a fixed order in either call.  Costs one more 32-bit
+ * reduction per contribution than qsa_backward.  Arguments, layouts and errors
+ * are those of qsa_backward; the accumulators live in the workspace. */
 QSA_API qsa_status qsa_backward_deterministic(const qsa_problem *problem, void *workspace, size_t ws_bytes,
                                               const void *q, const void *k, const void *v, const void *o,
                                               const float *lse, const void *dout, void *dq, void *dk, void *dv,

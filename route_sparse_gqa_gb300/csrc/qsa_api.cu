@@ -88,8 +88,8 @@ Layout make_layout(const qsa_problem *p) {
     off = align256(off + tiles * sizeof(int32_t));
     L.off_delta = off;
     off = align256(off + p->B * p->Hq * p->S_q * sizeof(float));
-    // dK/dV accumulators: fp32, or 64-bit fixed point for the deterministic backward.
-    const size_t kv_acc = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * sizeof(unsigned long long);
+    // dK/dV accumulators: fp32, or (deterministic backward) an fp32 and a 32-bit integer word per element.
+    const size_t kv_acc = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * 8;
     L.off_dk = off;
     off = align256(off + kv_acc);
     L.off_dv = off;
@@ -236,12 +236,14 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
     cudaError_t e;
     if (deterministic) {
         // Fixed-point accumulators in the workspace; the caller's fp32 buffers (if any) receive the sums.
-        b.dk_fx = at<unsigned long long>(ws, L.off_dk);
-        b.dv_fx = at<unsigned long long>(ws, L.off_dv);
+        b.dk_fx.est = at<float>(ws, L.off_dk);
+        b.dk_fx.lo = at<uint32_t>(ws, L.off_dk + n_kv * sizeof(float));
+        b.dv_fx.est = at<float>(ws, L.off_dv);
+        b.dv_fx.lo = at<uint32_t>(ws, L.off_dv + n_kv * sizeof(float));
         b.dk_acc = dk_f32;
         b.dv_acc = dv_f32;
-        e = cudaMemsetAsync(b.dk_fx, 0, n_kv * sizeof(unsigned long long), stream);
-        if (e == cudaSuccess) e = cudaMemsetAsync(b.dv_fx, 0, n_kv * sizeof(unsigned long long), stream);
+        e = cudaMemsetAsync(at<char>(ws, L.off_dk), 0, n_kv * 8, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(at<char>(ws, L.off_dv), 0, n_kv * 8, stream);
     } else {
         b.dk_acc = dk_f32 ? dk_f32 : at<float>(ws, L.off_dk);
         b.dv_acc = dv_f32 ? dv_f32 : at<float>(ws, L.off_dv);

@@ -80,7 +80,7 @@ struct BwdParams {
     const float *lse, *delta;
     __nv_bfloat16 *dq;
     float *dk_acc, *dv_acc;
-    unsigned long long *dk_fx, *dv_fx;  // deterministic mode: fixed-point accumulators
+    FxAcc dk_fx, dv_fx;  // deterministic mode: exact accumulators
     DeviceStatus *status;
 };
 
@@ -93,7 +93,7 @@ enum BarId {
     kDQReady, kDQFree, kDrain, kSFull
 };
 
-// kDet: the flush adds dK/dV as fixed-point integers (order-independent, bitwise reproducible sums).
+// kDet: the flush adds dK/dV into the exact accumulators (FxAcc: bitwise reproducible sums).
 template <bool kDet>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -452,8 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             const int64_t base_off = (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
             float *dk_base = kDet ? nullptr : p.dk_acc + base_off;
             float *dv_base = kDet ? nullptr : p.dv_acc + base_off;
-            unsigned long long *dk_fx_base = kDet ? p.dk_fx + base_off : nullptr;
-            unsigned long long *dv_fx_base = kDet ? p.dv_fx + base_off : nullptr;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 // The chunk's 64 keys, one pair per lane, broadcast below with shuffles.  The loop has no
                 // branch: a partial chunk's padding columns have empty membership, so their dK^T/dV^T
@@ -481,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                         const int32_t key = __shfl_sync(0xffffffffu, j < 32 ? key_lo : key_hi, j & 31);
                         const int64_t off = (int64_t)key * row_stride + h * 128;
                         if (kDet) {
-                            red_add_fx(dk_fx_base + off, __uint_as_float(a[j >> 5][j & 31]));
-                            red_add_fx(dv_fx_base + off, __uint_as_float(v[j >> 5][j & 31]));
+                            red_add_fx(p.dk_fx, base_off + off, __uint_as_float(a[j >> 5][j & 31]));
+                            red_add_fx(p.dv_fx, base_off + off, __uint_as_float(v[j >> 5][j & 31]));
                         } else {
                             red_add_f32(dk_base + off, __uint_as_float(a[j >> 5][j & 31]));
                             red_add_f32(dv_base + off, __uint_as_float(v[j >> 5][j & 31]));
@@ -564,7 +562,7 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
             for (int64_t gi = 0; gi < n_g; ++gi)
                 if (!tc_encode_kv_maps(&p.kv[b * n_g + gi], a, b, g0 + gi)) return cudaErrorInvalidValue;
         const int grid = (int)std::min<int64_t>(p.n_items, sms);
-        if (bw.dk_fx)
+        if (bw.dk_fx.est)
             tc_bwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
         else
             tc_bwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);

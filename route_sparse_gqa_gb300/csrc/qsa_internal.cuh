@@ -114,6 +114,33 @@ struct AttnArgs {
 
 cudaError_t launch_rowwise_forward(const AttnArgs &a, __nv_bfloat16 *o, float *lse, cudaStream_t s);
 
+// Deterministic dK/dV.  Every contribution x is rounded once to the integer
+// c = round(x * 2^24).  Two 32-bit reductions per element: `lo` sums c modulo
+// 2^32 (integer addition: exact and independent of order) and `est` sums x in
+// fp32 (order-dependent rounding, but within far less than 2^31 / 2^24 = 128 of
+// the exact sum).  The exact integer sum is the one value congruent to `lo`
+// modulo 2^32 nearest to est * 2^24, so the result depends on the inputs only:
+// bitwise reproducible.  Resolution 2^-24 per contribution.
+struct FxAcc {
+    float *est;    // [n] fp32 running sums
+    uint32_t *lo;  // [n] sums of round(x * 2^24) modulo 2^32
+};
+
+constexpr float kFxScale = 16777216.0f;  // 2^24
+
+__device__ __forceinline__ void red_add_fx(const FxAcc &acc, int64_t i, float x) {
+    const uint32_t c = (uint32_t)(unsigned long long)__float2ll_rn(x * kFxScale);
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(acc.est + i), "f"(x) : "memory");
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(acc.lo + i), "r"(c) : "memory");
+}
+
+__device__ __forceinline__ float fx_to_f32(float est, uint32_t lo) {
+    const double e = (double)est * (double)kFxScale;
+    const long long k = __double2ll_rn((e - (double)lo) * (1.0 / 4294967296.0));
+    const long long sum = (long long)lo + k * 4294967296ll;
+    return (float)((double)sum * (1.0 / (double)kFxScale));
+}
+
 struct BwdArgs {
     AttnArgs f;
     const __nv_bfloat16 *o, *dout;
@@ -121,29 +148,12 @@ struct BwdArgs {
     float *delta;  // [B, Hq, S_q]
     __nv_bfloat16 *dq, *dk, *dv;
     float *dk_acc, *dv_acc;  // fp32 [B, S_kv, Hkv, D]: the accumulators, or (deterministic) fp32 outputs / null
-    // Deterministic mode: fixed-point accumulators [B, S_kv, Hkv, D], else null.
-    unsigned long long *dk_fx, *dv_fx;
+    // Deterministic mode: exact accumulators (see FxAcc), else est = null.
+    FxAcc dk_fx, dv_fx;
 };
 
-// Deterministic dK/dV: every contribution x is added as the integer round(x * 2^32)
-// with a 64-bit integer reduction.  Integer addition is associative, so the sum
-// does not depend on the order in which the contributions arrive, and the result
-// is bitwise reproducible.  Resolution 2^-32 per contribution; the two's
-// complement sums are exact as long as each contribution and the final sum stay
-// below 2^31 in magnitude (intermediate wrap-around cancels).
-constexpr float kFxScale = 4294967296.0f;       // 2^32
-constexpr double kFxInvScale = 1.0 / 4294967296.0;
-
-__device__ __forceinline__ void red_add_fx(unsigned long long *addr, float x) {
-    const long long v = __float2ll_rn(x * kFxScale);
-    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ float fx_to_f32(unsigned long long v) {
-    return (float)((double)(long long)v * kFxInvScale);
-}
-cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s);  // deterministic when a.dk_fx is set
+cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s);  // deterministic when a.dk_fx.est is set
 cudaError_t launch_delta(const BwdArgs &a, cudaStream_t s);
-cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s);  // from a.dk_fx when set
+cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s);  // from a.dk_fx when a.dk_fx.est is set
 
 }  // namespace qsa

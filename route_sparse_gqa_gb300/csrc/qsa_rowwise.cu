@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(BwdArgs a) {
     }
 }
 
-// kDet: dK/dV contributions go to the fixed-point accumulators (order-independent sums).
+// kDet: dK/dV contributions go to the exact accumulators (FxAcc: order-independent sums).
 template <bool kDet>
 __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
     const AttnArgs &f = a.f;
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
                     const int64_t e0 = ((b * f.S_kv + j[u]) * f.Hkv + g) * kHeadDim + lane * 8;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        red_add_fx(a.dk_fx + e0 + i, c * qf[i]);
-                        red_add_fx(a.dv_fx + e0 + i, p * df[i]);
+                        red_add_fx(a.dk_fx, e0 + i, c * qf[i]);
+                        red_add_fx(a.dv_fx, e0 + i, p * df[i]);
                     }
                 } else {
                     float *dkj = dkbase + j[u] * f.Hkv * kHeadDim;
@@ -218,15 +218,15 @@ __global__ void convert_kernel(const float *dk, const float *dv, __nv_bfloat16 *
     }
 }
 
-// Fixed-point sums -> bf16 gradients, and fp32 copies when dk32/dv32 are given.
-__global__ void convert_fx_kernel(const unsigned long long *dk, const unsigned long long *dv, __nv_bfloat16 *dkb,
-                                  __nv_bfloat16 *dvb, float *dk32, float *dv32, int64_t n8) {
+// Exact sums -> bf16 gradients, and fp32 copies when dk32/dv32 are given.
+__global__ void convert_fx_kernel(FxAcc dk, FxAcc dv, __nv_bfloat16 *dkb, __nv_bfloat16 *dvb, float *dk32, float *dv32,
+                                  int64_t n8) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
         float kf[8], vf[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            kf[e] = fx_to_f32(dk[8 * i + e]);
-            vf[e] = fx_to_f32(dv[8 * i + e]);
+            kf[e] = fx_to_f32(dk.est[8 * i + e], dk.lo[8 * i + e]);
+            vf[e] = fx_to_f32(dv.est[8 * i + e], dv.lo[8 * i + e]);
         }
         reinterpret_cast<uint4 *>(dkb)[i] = f32x8_to_bf16(kf);
         reinterpret_cast<uint4 *>(dvb)[i] = f32x8_to_bf16(vf);
@@ -256,7 +256,7 @@ cudaError_t launch_delta(const BwdArgs &a, cudaStream_t s) {
 
 cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s) {
     dim3 grid((unsigned)(a.f.B * a.f.S_q), (unsigned)a.f.Hkv);
-    if (a.dk_fx)
+    if (a.dk_fx.est)
         rowwise_bwd_kernel<true><<<grid, kThreads, 0, s>>>(a);
     else
         rowwise_bwd_kernel<false><<<grid, kThreads, 0, s>>>(a);
@@ -267,7 +267,7 @@ cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s) {
     const int64_t n8 = a.f.B * a.f.S_kv * a.f.Hkv * kHeadDim / 8;
     int64_t nb = (n8 + 255) / 256;
     int blocks = (int)(nb < 152 * 16 ? nb : 152 * 16);
-    if (a.dk_fx)
+    if (a.dk_fx.est)
         convert_fx_kernel<<<blocks, 256, 0, s>>>(a.dk_fx, a.dv_fx, a.dk, a.dv, a.dk_acc, a.dv_acc, n8);
     else
         convert_kernel<<<blocks, 256, 0, s>>>(a.dk_acc, a.dv_acc, a.dk, a.dv, n8);
