@@ -450,8 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             if (it.nch == 0) continue;
             const int64_t row_stride = p.Hkv * kHeadDim;
             const int64_t base_off = (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
-            float *dk_base = kDet ? nullptr : p.dk_acc + base_off;
-            float *dv_base = kDet ? nullptr : p.dv_acc + base_off;
+            float *dk_base = kDet ? p.dk_fx.est + base_off : p.dk_acc + base_off;
+            float *dv_base = kDet ? p.dv_fx.est + base_off : p.dv_acc + base_off;
+            uint32_t *dk_lo = kDet ? p.dk_fx.lo + base_off : nullptr;
+            uint32_t *dv_lo = kDet ? p.dv_fx.lo + base_off : nullptr;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 // The chunk's 64 keys, one pair per lane, broadcast below with shuffles.  The loop has no
                 // branch: a partial chunk's padding columns have empty membership, so their dK^T/dV^T
@@ -479,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                         const int32_t key = __shfl_sync(0xffffffffu, j < 32 ? key_lo : key_hi, j & 31);
                         const int64_t off = (int64_t)key * row_stride + h * 128;
                         if (kDet) {
-                            red_add_fx(p.dk_fx, base_off + off, __uint_as_float(a[j >> 5][j & 31]));
-                            red_add_fx(p.dv_fx, base_off + off, __uint_as_float(v[j >> 5][j & 31]));
+                            red_add_fx(dk_base + off, dk_lo + off, __uint_as_float(a[j >> 5][j & 31]));
+                            red_add_fx(dv_base + off, dv_lo + off, __uint_as_float(v[j >> 5][j & 31]));
                         } else {
                             red_add_f32(dk_base + off, __uint_as_float(a[j >> 5][j & 31]));
                             red_add_f32(dv_base + off, __uint_as_float(v[j >> 5][j & 31]));

@@ -128,11 +128,13 @@ struct FxAcc {
 
 constexpr float kFxScale = 16777216.0f;  // 2^24
 
-__device__ __forceinline__ void red_add_fx(const FxAcc &acc, int64_t i, float x) {
+__device__ __forceinline__ void red_add_fx(float *est, uint32_t *lo, float x) {
     const uint32_t c = (uint32_t)(unsigned long long)__float2ll_rn(x * kFxScale);
-    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(acc.est + i), "f"(x) : "memory");
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(acc.lo + i), "r"(c) : "memory");
+    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(est), "f"(x) : "memory");
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(lo), "r"(c) : "memory");
 }
+
+__device__ __forceinline__ void red_add_fx(const FxAcc &acc, int64_t i, float x) { red_add_fx(acc.est + i, acc.lo + i, x); }
 
 __device__ __forceinline__ float fx_to_f32(float est, uint32_t lo) {
     const double e = (double)est * (double)kFxScale;
