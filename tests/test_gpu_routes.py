@@ -366,3 +366,33 @@ def test_forced_wait_timeout_in_the_score_kernel_is_reported():
     qd, kd = f64(case.q), f64(case.k)
     ref = oracle.index_scores(qd, kd, w.c, w.offset)
     _assert_valid_topk(got, ref, _score_tol(qd, kd, ref), case.lengths, w.budget, w.c, w.offset)
+
+
+def test_strided_index_queries_from_a_fused_projection():
+    """The indexer's fused projection yields [B, S, (H + 1) * D]; the queries are a
+    strided view of its first H heads.  The producer takes the view as it is and
+    returns exactly what it returns for a contiguous copy."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    rng = W.rng_for(0, seed=99)
+    B, S, H, D, c, budget = 2, 700, 16, 64, 4, 96
+    fused = W.bf16_normal(rng, (B, S, (H + 1) * D))
+    kb = W.bf16_normal(rng, (B, S // c, 1, D))
+    dev = _dev()
+    f = bf16_to_device(fused, dev)
+    q_view = f.view(B, S, H + 1, D)[:, :, :H]
+    assert not q_view.is_contiguous()
+    k = bf16_to_device(kb, dev)
+    lens = torch.tensor([S, 555], dtype=torch.int64, device=dev)
+    a = qsa.select_qsa_token_ids(q_view, k, lens, budget, c)
+    b = qsa.select_qsa_token_ids(q_view.contiguous(), k, lens, budget, c)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    ids = a.cpu().numpy()
+    _row_structure(ids, [S, 555], budget, c, 0, S // c)
+    qd = f64(np.ascontiguousarray(fused.reshape(B, S, H + 1, D)[:, :, :H]))
+    kd = f64(kb)
+    ref = oracle.index_scores(qd, kd, c)
+    _assert_valid_topk(ids, ref, _score_tol(qd, kd, ref), np.array([S, 555]), budget, c, 0)
