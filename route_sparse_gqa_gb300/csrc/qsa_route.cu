@@ -866,6 +866,14 @@ qsa_status qsa_select_token_ids(const qsa_route_problem *p, const void *q, const
     if (st != QSA_OK) return st;
     const size_t id_bytes = (size_t)p->B * p->S_q * (p->token_budget + p->compress_ratio - 1) * sizeof(int32_t);
     if (overlaps(ids, id_bytes, ws, need)) return route_fail(QSA_ERR_INVALID_ARGUMENT, "ids overlap the workspace");
+    const size_t q_bytes = 2 * (size_t)((p->B - 1) * p->q_stride[0] + (p->S_q - 1) * p->q_stride[1] +
+                                        (p->H_index - 1) * p->q_stride[2] + p->D_index);
+    const size_t k_bytes = p->n_blocks > 0 ? 2 * (size_t)((p->B - 1) * p->k_stride[0] +
+                                                          (p->n_blocks - 1) * p->k_stride[1] + p->D_index)
+                                           : 0;
+    if (overlaps(ids, id_bytes, q, q_bytes) || (k && overlaps(ids, id_bytes, k, k_bytes)) ||
+        overlaps(ids, id_bytes, seq_len, (size_t)p->B * sizeof(int64_t)))
+        return route_fail(QSA_ERR_INVALID_ARGUMENT, "ids overlap an input");
     float *scores = reinterpret_cast<float *>(static_cast<char *>(ws) + kOffScores);
     st = launch_scores(p, q, k, seq_len, ws, scores, stream);
     if (st != QSA_OK) return st;

@@ -88,13 +88,10 @@ bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, 
 }
 
 bool tc_head_major_order(const AttnArgs &a, int64_t n_g) {
-    static int64_t l2 = -1;
-    if (l2 < 0) {
-        int dev = 0, bytes = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&bytes, cudaDevAttrL2CacheSize, dev);
-        l2 = bytes > 0 ? bytes : (64ll << 20);
-    }
+    int dev = 0, bytes = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&bytes, cudaDevAttrL2CacheSize, dev);
+    const int64_t l2 = bytes > 0 ? bytes : (64ll << 20);
     const int64_t acc_bytes = a.B * a.S_kv * n_g * kHeadDim * 2 * (int64_t)sizeof(float);
     return acc_bytes > l2 / 2;
 }
