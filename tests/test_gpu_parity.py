@@ -85,6 +85,20 @@ def test_small_shapes(B, S_q, S_kv, Hq, Hkv, K, pattern, dtype):
     _full_compare(q, k, v, do, routes, 1.0 / 16, S_kv)
 
 
+def test_maximum_route_slots():
+    """K = 16384 route slots (the library's maximum) with duplicates and invalid
+    values, over 20000 keys: the uncached route-row path and tiles of ~300 chunks."""
+    rng = np.random.default_rng(16384)
+    B, S_q, S_kv, Hq, Hkv, K = 1, 20, 20000, 16, 2, 16384
+    q = W.bf16_normal(rng, (B, S_q, Hq, 256))
+    k = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
+    v = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
+    do = W.bf16_normal(rng, (B, S_q, Hq, 256))
+    routes = rng.integers(-5, S_kv + 5, size=(B, S_q, K)).astype(np.int32)
+    routes[0, 3] = -1  # an empty row
+    _full_compare(q, k, v, do, routes, 1.0 / 16, S_kv)
+
+
 def test_all_rows_empty():
     q, k, v, do, routes = _random_case(3, 1, 40, 64, 16, 2, 8, p_empty=1.0)
     out = _full_compare(q, k, v, do, routes, 0.1, 64)
