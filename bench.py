@@ -16,9 +16,11 @@ has) on a bounded sample of the same workload, on the host cores.
 ``--route-producer`` measures the route producer instead (compressed-block
 index scores + top-k selection, ``select_qsa_token_ids``) on the training-step
 index workload (B=1, S=32768, H_index=32, D_index=128, c=4, budget 2048): one
-step = the score kernel and the selection kernel through the C ABI; ``value`` is
-useful TFLOP/s of the scoring (2*H*D per visible (row, block) pair) over the
-whole step.  With ``--impl reference`` it times the oracle on sampled rows.
+step = one ``qsa_select_token_ids`` call (score kernel + selection kernel);
+``value`` is useful TFLOP/s of the scoring (2*H*D per visible (row, block)
+pair) over the whole step.  The score kernel is also timed alone; the
+selection's time is the step's minus that.  With ``--impl reference`` it times
+the oracle on sampled rows.
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the
 path needs no exchange); the barrier and the max-over-ranks timing use
@@ -565,22 +567,26 @@ def run_route_producer(args):
     pairs, flop, live_rows = route_work(w, case.lengths)
 
     def step(ev=None):
+        # The product call: scores into the workspace, then the selection.
         if ev:
             ev[0].record()
-        _abi.check(lib.qsa_index_scores(ctypes.byref(prob), qq.data_ptr(), kk.data_ptr(), lens.data_ptr(),
-                                        ws.data_ptr(), ws_bytes, scores_ptr, stream))
+        _abi.check(lib.qsa_select_token_ids(ctypes.byref(prob), qq.data_ptr(), kk.data_ptr(), lens.data_ptr(),
+                                            ws.data_ptr(), ws_bytes, ids.data_ptr(), stream))
         if ev:
             ev[1].record()
-        _abi.check(lib.qsa_select_from_scores(ctypes.byref(prob), scores_ptr, lens.data_ptr(), ws.data_ptr(),
-                                              ws_bytes, ids.data_ptr(), stream))
-        if ev:
-            ev[2].record()
+
+    def scores_only(ev):
+        ev[0].record()
+        _abi.check(lib.qsa_index_scores(ctypes.byref(prob), qq.data_ptr(), kk.data_ptr(), lens.data_ptr(),
+                                        ws.data_ptr(), ws_bytes, scores_ptr, stream))
+        ev[1].record()
 
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()
     _abi.check(lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream)))
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -589,12 +595,17 @@ def run_route_producer(args):
             flush.fill_(i & 0xFF)
             step(events[i])
         torch.cuda.synchronize()
+        # The score kernel alone (same launches as inside the product call), for the breakdown.
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            scores_only(sev[i])
+        torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    per = np.array([[events[i][0].elapsed_time(events[i][1]), events[i][1].elapsed_time(events[i][2])]
-                    for i in range(args.steps)])
-    score_ms, sel_ms = (float(x) for x in per.mean(0))
-    step_ms = max_over_ranks(score_ms + sel_ms, dev)
+    local_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in events]))
+    score_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in sev]))
+    sel_ms = max(local_ms - score_ms, 1e-6)  # the selection and the launch between the kernels
+    step_ms = max_over_ranks(local_ms, dev)
     value = job_tflops(flop, world, step_ms)
     _abi.check(lib.qsa_read_device_status(ctypes.c_void_p(ws.data_ptr()), ctypes.c_void_p(stream)))
 

@@ -345,6 +345,14 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
+// Key of a score.  The fused path's scores are relu-sums times a positive
+// factor, never negative and never -0, and the bits of a non-negative float
+// are already order-preserving.
+template <bool kNonNeg>
+__device__ __forceinline__ uint32_t key_of(float f) {
+    return kNonNeg ? __float_as_uint(f) : score_key(f);
+}
+
 // Block-wide exclusive prefix sum of one 32-bit value per thread; `total` gets
 // the sum over the block.  Contains two barriers.
 __device__ __forceinline__ uint32_t block_scan(uint32_t x, uint32_t *warp_tot, uint32_t &total) {
@@ -432,6 +440,7 @@ __device__ __forceinline__ float4 load_once4(const float *p) {
 // segment of a 16-byte aligned row is read with 16-byte loads: the 32 lanes of
 // a warp read 32 different 128-byte lines per instruction, so wide loads cut
 // the L1 transactions fourfold.
+template <bool kNonNeg>
 __device__ __forceinline__ int load_segment(const float *srow, uint32_t nvis, uint32_t ch,
                                             uint32_t (&k)[kKeysPerThread], bool aligned16) {
     const uint32_t i0 = ch * (uint32_t)kSelChunk + threadIdx.x * kKeysPerThread;
@@ -440,14 +449,14 @@ __device__ __forceinline__ int load_segment(const float *srow, uint32_t nvis, ui
 #pragma unroll
         for (int j = 0; j < kKeysPerThread; j += 4) {
             const float4 v = load_once4(srow + i0 + j);
-            k[j] = score_key(v.x);
-            k[j + 1] = score_key(v.y);
-            k[j + 2] = score_key(v.z);
-            k[j + 3] = score_key(v.w);
+            k[j] = key_of<kNonNeg>(v.x);
+            k[j + 1] = key_of<kNonNeg>(v.y);
+            k[j + 2] = key_of<kNonNeg>(v.z);
+            k[j + 3] = key_of<kNonNeg>(v.w);
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < kKeysPerThread; ++j) k[j] = j < n ? score_key(load_once(srow + i0 + j)) : 0u;
+        for (int j = 0; j < kKeysPerThread; ++j) k[j] = j < n ? key_of<kNonNeg>(load_once(srow + i0 + j)) : 0u;
     }
     return n;
 }
@@ -466,6 +475,7 @@ __device__ __forceinline__ void clear_hist(uint32_t *hist) {
 }
 
 // Grid (S_q, B): one CTA per query row.
+template <bool kNonNeg>
 __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams p) {
     // One dynamic region, used in turn: a padded transposition buffer for the
     // row's keys while they load; then two digit histograms, the candidate keys
@@ -506,12 +516,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
                 uint32_t *dst = region + tid + (tid >> 5);  // slot of key tid; key tid + 256 j is 264 j further
                 if (nvis == (uint32_t)kSelChunk) {
 #pragma unroll
-                    for (int j = 0; j < kKeysPerThread; ++j) dst[j * 264] = score_key(__ldg(src + j * kSelThreads));
+                    for (int j = 0; j < kKeysPerThread; ++j) dst[j * 264] = key_of<kNonNeg>(__ldg(src + j * kSelThreads));
                 } else {
 #pragma unroll
                     for (int j = 0; j < kKeysPerThread; ++j)
                         if ((uint32_t)j * kSelThreads + tid < nvis)
-                            dst[j * 264] = score_key(__ldg(src + j * kSelThreads));
+                            dst[j * 264] = key_of<kNonNeg>(__ldg(src + j * kSelThreads));
                 }
                 __syncthreads();
                 const uint32_t i0 = (uint32_t)tid * kKeysPerThread;
@@ -544,7 +554,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
                     }
                 } else {
                     for (uint32_t ch = 0; ch < n_chunks; ++ch) {
-                        if (!resident) n = load_segment(srow, nvis, ch, k, a16);
+                        if (!resident) n = load_segment<kNonNeg>(srow, nvis, ch, k, a16);
                         if (pass == 0) {
 #pragma unroll
                             for (int j = 0; j < kKeysPerThread; ++j)
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const SelParams 
             uint32_t sel_run = 0, eq_run = 0;
             const bool vec4 = staged && p.c == 4;  // whole 16-byte stores into the staged row
             for (uint32_t ch = 0; ch < n_chunks; ++ch) {
-                if (!resident) n = load_segment(srow, nvis, ch, k, a16);
+                if (!resident) n = load_segment<kNonNeg>(srow, nvis, ch, k, a16);
                 uint32_t gt_mask = 0, eq_mask = 0;  // bit j: key j of the segment
                 if (use_cand) {
                     // Keys in better bins than the first pass's are all > T; only this
@@ -787,8 +797,9 @@ qsa_status launch_scores(const qsa_route_problem *pr, const void *q, const void 
     }
 }
 
+// nonneg: the scores are known to be >= +0 (they come from the score kernel).
 qsa_status launch_select(const qsa_route_problem *pr, const float *scores, const int64_t *seq_len, int32_t *ids,
-                         cudaStream_t stream) {
+                         bool nonneg, cudaStream_t stream) {
     SelParams p;
     p.scores = scores;
     p.seq_len = seq_len;
@@ -802,11 +813,16 @@ qsa_status launch_select(const qsa_route_problem *pr, const float *scores, const
     const size_t smem = select_smem_words(p.W) * sizeof(uint32_t);
     if (smem > 48 * 1024) {
         qsa_status st = cuda_status(
-            cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+            nonneg ? cudaFuncSetAttribute(select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                   : cudaFuncSetAttribute(select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
             "cudaFuncSetAttribute");
         if (st != QSA_OK) return st;
     }
-    select_kernel<<<dim3((unsigned)pr->S_q, (unsigned)pr->B), kSelThreads, smem, stream>>>(p);
+    const dim3 grid((unsigned)pr->S_q, (unsigned)pr->B);
+    if (nonneg)
+        select_kernel<true><<<grid, kSelThreads, smem, stream>>>(p);
+    else
+        select_kernel<false><<<grid, kSelThreads, smem, stream>>>(p);
     return cuda_status(cudaGetLastError(), "selection kernel launch");
 }
 
@@ -852,7 +868,7 @@ qsa_status qsa_select_from_scores(const qsa_route_problem *p, const float *score
     if (!scores || !seq_len || !ids) return route_fail(QSA_ERR_INVALID_ARGUMENT, "null tensor pointer");
     st = check_route_ws(p, ws, ws_bytes, kOffScores);
     if (st != QSA_OK) return st;
-    return launch_select(p, scores, seq_len, ids, stream);
+    return launch_select(p, scores, seq_len, ids, false, stream);
 }
 
 qsa_status qsa_select_token_ids(const qsa_route_problem *p, const void *q, const void *k, const int64_t *seq_len,
@@ -877,7 +893,7 @@ qsa_status qsa_select_token_ids(const qsa_route_problem *p, const void *q, const
     float *scores = reinterpret_cast<float *>(static_cast<char *>(ws) + kOffScores);
     st = launch_scores(p, q, k, seq_len, ws, scores, stream);
     if (st != QSA_OK) return st;
-    return launch_select(p, scores, seq_len, ids, stream);
+    return launch_select(p, scores, seq_len, ids, true, stream);
 }
 
 }  // extern "C"
