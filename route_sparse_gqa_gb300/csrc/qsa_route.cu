@@ -64,13 +64,13 @@ constexpr int kScoreThreads = 320;  // warp 0 producer, 1 MMA, 2-9 epilogue
 constexpr int kEpiThreads = 256;
 constexpr int kBlkTile = 128;  // blocks per tile (MMA M)
 constexpr int kRowsN = 256;    // (query, head) rows per item (MMA N)
-constexpr int kScoreStages = 4;
+constexpr int kScoreStages = 3;  // K tile ring (two Q tiles take the rest of shared memory)
 constexpr int kMaxIndexDim = 128;
 constexpr uint32_t kTmemCols = 512;  // two accumulators of 256 fp32 columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Barrier slots.
-enum { kBarQFull, kBarQEmpty, kBarDrain, kBarKFull, kBarKEmpty = kBarKFull + kScoreStages,
+enum { kBarQFull, kBarQEmpty = kBarQFull + 2, kBarDrain = kBarQEmpty + 2, kBarKFull, kBarKEmpty = kBarKFull + kScoreStages,
        kBarAccFull = kBarKEmpty + kScoreStages, kBarAccEmpty = kBarAccFull + 2, kBarItemFull = kBarAccEmpty + 2,
        kBarItemEmpty = kBarItemFull + kQueueRing, kNumScoreBars = kBarItemEmpty + kQueueRing };
 
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
     const uint32_t k_panel = kBlkTile * 128;  // one 64-column panel of a K tile
     const int n_panels = (int)(p.D / 64);
     const uint32_t q_bytes = q_panel * n_panels, k_bytes = k_panel * n_panels;
-    const uint32_t off_k = q_bytes;
+    const uint32_t off_k = 2 * q_bytes;  // two Q tiles: the next item's loads while this one computes
     const uint32_t off_bar = off_k + kScoreStages * k_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + off_bar);
     uint8_t *misc = smem + off_bar + kNumScoreBars * 8;
@@ -131,8 +131,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
     const uint32_t sbase = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        mbar_init(bars + kBarQFull, 1);
-        mbar_init(bars + kBarQEmpty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bars + kBarQFull + b, 1);
+            mbar_init(bars + kBarQEmpty + b, 1);
+        }
         mbar_init(bars + kBarDrain, 1);
         for (int s = 0; s < kScoreStages; ++s) {
             mbar_init(bars + kBarKFull + s, 1);
@@ -180,13 +182,18 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
                 const ScoreItem it = score_item(p, idx);
                 if (it.n_kt == 0) continue;
                 // The Q tile is reused once the previous item's last MMAs have completed.
-                if (nq > 0 && !mbar_wait(bars + kBarQEmpty, (uint32_t)((nq - 1) & 1), abort_flag, p.wait_limit_ns)) {
+                // Q tiles alternate between two buffers; a buffer is reused once the MMAs of the item two
+                // back, its previous user, have completed.
+                const int qb = (int)(nq & 1);
+                if (nq >= 2 &&
+                    !mbar_wait(bars + kBarQEmpty + qb, (uint32_t)((nq / 2 - 1) & 1), abort_flag, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bars + kBarQFull, q_bytes);
+                mbar_arrive_expect_tx(bars + kBarQFull + qb, q_bytes);
                 for (int kb = 0; kb < n_panels; ++kb)
-                    tma_load_4d(sbase + kb * q_panel, &p.q_map, bars + kBarQFull, kb * 64, 0, (int)it.t0, (int)it.b);
+                    tma_load_4d(sbase + qb * q_bytes + kb * q_panel, &p.q_map, bars + kBarQFull + qb, kb * 64, 0,
+                                (int)it.t0, (int)it.b);
                 ++nq;
                 for (int kt = 0; kt < it.n_kt; ++kt, ++gk) {
                     const int s = (int)(gk % kScoreStages);
@@ -206,7 +213,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
             queue_finish(p.sched);
             // Drain: every issued copy must have landed before the CTA leaves.
             bool drained = true;
-            if (nq > 0) drained &= mbar_wait(bars + kBarQFull, (uint32_t)((nq - 1) & 1), &zero, kWaitLimitNs);
+            for (int64_t g = nq > 2 ? nq - 2 : 0; g < nq; ++g)
+                drained &= mbar_wait(bars + kBarQFull + (int)(g & 1), (uint32_t)((g / 2) & 1), &zero, kWaitLimitNs);
             for (int64_t g = gk > kScoreStages ? gk - kScoreStages : 0; g < gk; ++g)
                 drained &= mbar_wait(bars + kBarKFull + (int)(g % kScoreStages),
                                      (uint32_t)((g / kScoreStages) & 1), &zero, kWaitLimitNs);
@@ -226,7 +234,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
                 if (!ok || idx < 0) break;
                 const ScoreItem it = score_item(p, idx);
                 if (it.n_kt == 0) continue;
-                if (!mbar_wait(bars + kBarQFull, (uint32_t)(nq & 1), abort_flag, p.wait_limit_ns)) {
+                const int qb = (int)(nq & 1);
+                if (!mbar_wait(bars + kBarQFull + qb, (uint32_t)((nq / 2) & 1), abort_flag, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -246,7 +255,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint64_t ad = sdesc_sw128(kt_base + kb * k_panel + k * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(sbase + kb * q_panel + k * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(sbase + qb * q_bytes + kb * q_panel + k * 32, 16, 1024);
                             mma_bf16(tmem + a * 256, ad, bd, idesc, (kb | k) ? 1u : 0u);
                         }
                     }
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) index_score_kernel(const __g
                     mma_commit(bars + kBarAccFull + a);
                 }
                 if (!ok) break;
-                mma_commit(bars + kBarQEmpty);
+                mma_commit(bars + kBarQEmpty + qb);
                 ++nq;
             }
             if (!ok) fail(3);
@@ -733,7 +742,7 @@ qsa_status cuda_status(cudaError_t e, const char *what) {
 
 uint32_t score_smem_bytes(int64_t D) {
     const uint32_t panels = (uint32_t)(D / 64);
-    return panels * (kRowsN * 128 + kScoreStages * kBlkTile * 128) + kNumScoreBars * 8 + 64 + 1024;
+    return panels * (2 * kRowsN * 128 + kScoreStages * kBlkTile * 128) + kNumScoreBars * 8 + 64 + 1024;
 }
 
 template <int H>
