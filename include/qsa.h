@@ -51,7 +51,7 @@ extern "C" {
 typedef enum qsa_status {
     QSA_OK = 0,
     QSA_ERR_INVALID_ARGUMENT = 1,    /* empty dim, Hq % Hkv != 0, bad scale, null or aliasing pointer, bad route_bits */
-    QSA_ERR_UNSUPPORTED = 2,         /* D != 256, S_kv > 2^31 - 1, K > 16384, non-unit last stride, misaligned */
+    QSA_ERR_UNSUPPORTED = 2,         /* D not 64/128/256, S_kv > 2^31 - 1, K > 16384, non-unit last stride, misaligned */
     QSA_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < qsa_workspace_bytes(problem) */
     QSA_ERR_CUDA = 4,                /* a CUDA runtime call or kernel launch failed */
     QSA_ERR_TIMEOUT = 5,             /* a device-side wait hit its iteration limit (reported by qsa_read_device_status) */
@@ -63,8 +63,9 @@ typedef enum qsa_status {
  *   Q, O, dO, dQ : [B, S_q, Hq, D]      K, V, dK, dV : [B, S_kv, Hkv, D]
  *   routes       : [B, S_q, K] signed int32 or int64 (route_bits = 32 or 64)
  *   LSE          : [B, Hq, S_q] float32, natural log
- * Hq must be a positive multiple of Hkv; D must be 256 (fa4_sparse_gqa_attention
- * fixes head_dim = 256).  S_kv may differ from S_q (context parallelism: local
+ * Hq must be a positive multiple of Hkv.  D is 256 as fa4_sparse_gqa_attention
+ * fixes head_dim = 256 (the tensor-core tile kernels); D = 64 and 128 are also
+ * accepted and run on the warp-level kernels.  S_kv may differ from S_q (context parallelism: local
  * queries against gathered global K/V).  softmax_scale must be finite and > 0;
  * the pages' default 1/sqrt(D) is resolved by the caller.
  * Strides are in elements.  q/k/v need a unit last stride and, for the other

@@ -43,7 +43,8 @@ qsa_status validate(const qsa_problem *p) {
                     (double)p->softmax_scale);
     if (p->route_bits != 32 && p->route_bits != 64)
         return fail(QSA_ERR_INVALID_ARGUMENT, "route_bits must be 32 or 64 (got %d)", p->route_bits);
-    if (p->D != kHeadDim) return fail(QSA_ERR_UNSUPPORTED, "head dim D=%lld: only D=256 is supported", (long long)p->D);
+    if (p->D != 64 && p->D != 128 && p->D != kHeadDim)
+        return fail(QSA_ERR_UNSUPPORTED, "head dim D=%lld: 64, 128 or 256 is supported", (long long)p->D);
     if (p->S_kv > 2147483647LL) return fail(QSA_ERR_UNSUPPORTED, "S_kv=%lld exceeds 2^31-1", (long long)p->S_kv);
     if (p->K > kMaxRouteSlots)
         return fail(QSA_ERR_UNSUPPORTED, "K=%lld route slots exceeds %d", (long long)p->K, kMaxRouteSlots);
@@ -63,7 +64,8 @@ qsa_status validate(const qsa_problem *p) {
 Layout make_layout(const qsa_problem *p) {
     Layout L{};
     L.G = p->Hq / p->Hkv;
-    L.T = (is_pow2(L.G) && L.G >= 4 && L.G <= kTileRows) ? kTileRows / L.G : 0;
+    // The tile path covers D = 256 and power-of-two groups of 4..64 heads; the rest runs warp-level.
+    L.T = (p->D == kHeadDim && is_pow2(L.G) && L.G >= 4 && L.G <= kTileRows) ? kTileRows / L.G : 0;
     L.n_tiles = L.T ? (p->S_q + L.T - 1) / L.T : 0;
     const int64_t union_cap = L.T ? std::min<int64_t>(L.T * p->K, p->S_kv) : 0;
     L.max_chunks = (union_cap + kChunkKeys - 1) / kChunkKeys;
@@ -89,7 +91,7 @@ Layout make_layout(const qsa_problem *p) {
     L.off_delta = off;
     off = align256(off + p->B * p->Hq * p->S_q * sizeof(float));
     // dK/dV accumulators: fp32, or (deterministic backward) an fp32 and a 32-bit integer word per element.
-    const size_t kv_acc = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim * 8;
+    const size_t kv_acc = (size_t)p->B * p->S_kv * p->Hkv * p->D * 8;
     L.off_dk = off;
     off = align256(off + kv_acc);
     L.off_dv = off;
@@ -122,9 +124,10 @@ qsa_status check_ws(const qsa_problem *p, const void *ws, size_t ws_bytes, Layou
 bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
 // [lo, hi) byte range of a strided [B, S, H, D] bf16 tensor.
-void span_of(const void *base, const int64_t *stride, int64_t B, int64_t S, int64_t H, uintptr_t &lo, uintptr_t &hi) {
+void span_of(const void *base, const int64_t *stride, int64_t B, int64_t S, int64_t H, int64_t D, uintptr_t &lo,
+             uintptr_t &hi) {
     lo = reinterpret_cast<uintptr_t>(base);
-    hi = lo + 2 * (size_t)((B - 1) * stride[0] + (S - 1) * stride[1] + (H - 1) * stride[2] + kHeadDim);
+    hi = lo + 2 * (size_t)((B - 1) * stride[0] + (S - 1) * stride[1] + (H - 1) * stride[2] + D);
 }
 
 bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
@@ -139,6 +142,7 @@ AttnArgs attn_args(const qsa_problem *p, const Layout &L, const void *ws, const 
     a.Hkv = p->Hkv;
     a.K = p->K;
     a.G = L.G;
+    a.D = p->D;
     a.scale = p->softmax_scale;
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.k = static_cast<const __nv_bfloat16 *>(k);
@@ -195,11 +199,11 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
     if ((dk_f32 && !aligned16(dk_f32)) || (dv_f32 && !aligned16(dv_f32)))
         return fail(QSA_ERR_UNSUPPORTED, "fp32 accumulators must be 16-byte aligned");
     uintptr_t q0, q1, k0, k1, v0, v1;
-    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, q0, q1);
-    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, k0, k1);
-    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, v0, v1);
-    const size_t nq = 2 * (size_t)(p->B * p->S_q * p->Hq * kHeadDim);
-    const size_t nkv = 2 * (size_t)(p->B * p->S_kv * p->Hkv * kHeadDim);
+    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, p->D, q0, q1);
+    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, p->D, k0, k1);
+    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, p->D, v0, v1);
+    const size_t nq = 2 * (size_t)(p->B * p->S_q * p->Hq * p->D);
+    const size_t nkv = 2 * (size_t)(p->B * p->S_kv * p->Hkv * p->D);
     auto u = [](const void *x) { return reinterpret_cast<uintptr_t>(x); };
     const uintptr_t ins[6][2] = {{q0, q1}, {k0, k1}, {v0, v1}, {u(o), u(o) + nq}, {u(dout), u(dout) + nq},
                                  {u(lse), u(lse) + 4 * (size_t)(p->B * p->Hq * p->S_q)}};
@@ -232,7 +236,7 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
     b.dq = static_cast<__nv_bfloat16 *>(dq);
     b.dk = static_cast<__nv_bfloat16 *>(dk);
     b.dv = static_cast<__nv_bfloat16 *>(dv);
-    const size_t n_kv = (size_t)p->B * p->S_kv * p->Hkv * kHeadDim;
+    const size_t n_kv = (size_t)p->B * p->S_kv * p->Hkv * p->D;
     cudaError_t e;
     if (deterministic) {
         // Fixed-point accumulators in the workspace; the caller's fp32 buffers (if any) receive the sums.
@@ -334,10 +338,10 @@ qsa_status qsa_forward(const qsa_problem *p, void *ws, size_t ws_bytes, const vo
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
         return fail(QSA_ERR_UNSUPPORTED, "q, k, v and o must be 16-byte aligned");
     uintptr_t q0, q1, k0, k1, v0, v1;
-    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, q0, q1);
-    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, k0, k1);
-    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, v0, v1);
-    const uintptr_t o0 = reinterpret_cast<uintptr_t>(o), o1 = o0 + 2 * (size_t)(p->B * p->S_q * p->Hq * kHeadDim);
+    span_of(q, p->q_stride, p->B, p->S_q, p->Hq, p->D, q0, q1);
+    span_of(k, p->k_stride, p->B, p->S_kv, p->Hkv, p->D, k0, k1);
+    span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, p->D, v0, v1);
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(o), o1 = o0 + 2 * (size_t)(p->B * p->S_q * p->Hq * p->D);
     const uintptr_t l0 = reinterpret_cast<uintptr_t>(lse), l1 = l0 + 4 * (size_t)(p->B * p->Hq * p->S_q);
     const uintptr_t w0 = reinterpret_cast<uintptr_t>(ws), w1 = w0 + L.total;
     const uintptr_t in[4][2] = {{q0, q1}, {k0, k1}, {v0, v1}, {w0, w1}};

@@ -9,7 +9,7 @@
 
 namespace qsa {
 
-constexpr int kHeadDim = 256;        // fa4_sparse_gqa_attention fixes D = 256
+constexpr int kHeadDim = 256;        // fa4_sparse_gqa_attention fixes D = 256 (the tile kernels' head dim)
 constexpr int kChunkKeys = 64;       // keys per gathered chunk (one tensor-core N tile)
 constexpr int kTileRows = 128;       // (query, head) rows per tile = tcgen05 M
 constexpr int kMaxRouteSlots = 16384;  // per-row sort capacity (smem bitonic sort)
@@ -105,6 +105,7 @@ cudaError_t launch_route_tiles(const TilesArgs &a, cudaStream_t s);
 
 struct AttnArgs {
     int64_t B, S_q, S_kv, Hq, Hkv, K, G;
+    int64_t D;  // head dim: 256 on the tile path; 64, 128 or 256 on the warp-level path
     float scale;
     const __nv_bfloat16 *q, *k, *v;
     int64_t qs0, qs1, qs2, ks0, ks1, ks2, vs0, vs1, vs2;

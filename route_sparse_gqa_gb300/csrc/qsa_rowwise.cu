@@ -3,7 +3,8 @@
 // This is the general path: any group size G = Hq/Hkv, any route pattern.  A
 // CTA owns one (b, q, KV head g); its warps take the group's query heads, so the
 // K/V rows they gather for the row's route set are shared through L1.  Each
-// lane holds 8 of the 256 head dimensions.  Scores are warp-reduced dot
+// lane holds 8 consecutive head dimensions (D = 64, 128 or 256: the first D/8
+// lanes hold data, the others zeros, so the warp sums are unchanged).  Scores are warp-reduced dot
 // products, the softmax is online in fp32 (base-2 exponent with the scale
 // folded in), and LSE is reported in natural-log units.
 //
@@ -35,12 +36,13 @@ __global__ void __launch_bounds__(kThreads) rowwise_fwd_kernel(AttnArgs a, __nv_
     const int n = a.counts[row];
     const int32_t *R = a.ids + row * a.K;
     const float sl2 = a.scale * kLog2e;
+    const bool dl = lane * 8 < a.D;  // this lane holds head dimensions
     const __nv_bfloat16 *kbase = a.k + b * a.ks0 + g * a.ks2 + lane * 8;
     const __nv_bfloat16 *vbase = a.v + b * a.vs0 + g * a.vs2 + lane * 8;
     for (int64_t hl = warp; hl < a.G; hl += kWarps) {
         const int64_t h = g * a.G + hl;
         float qf[8], acc[8];
-        bf16x8_to_f32(ldg16(a.q + b * a.qs0 + qpos * a.qs1 + h * a.qs2 + lane * 8), qf);
+        bf16x8_to_f32(dl ? ldg16(a.q + b * a.qs0 + qpos * a.qs1 + h * a.qs2 + lane * 8) : make_uint4(0, 0, 0, 0), qf);
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
         float m = -INFINITY, l = 0.f;
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_fwd_kernel(AttnArgs a, __nv_
                     j[u] = -1;
                 }
                 float part = 0.f;
-                if (j[u] >= 0) {
+                if (j[u] >= 0 && dl) {
                     float kf[8];
                     bf16x8_to_f32(ldg16(kbase + j[u] * a.ks1), kf);
 #pragma unroll
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_fwd_kernel(AttnArgs a, __nv_
                 const float p = exp2f(s[u] - mx);
                 l += p;
                 float vf[8];
-                bf16x8_to_f32(ldg16(vbase + j[u] * a.vs1), vf);
+                bf16x8_to_f32(dl ? ldg16(vbase + j[u] * a.vs1) : make_uint4(0, 0, 0, 0), vf);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[i] = fmaf(p, vf[i], acc[i]);
             }
@@ -94,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_fwd_kernel(AttnArgs a, __nv_
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] *= inv;
-        *reinterpret_cast<uint4 *>(o + ((row * a.Hq + h) * kHeadDim + lane * 8)) = f32x8_to_bf16(acc);
+        if (dl) *reinterpret_cast<uint4 *>(o + ((row * a.Hq + h) * a.D + lane * 8)) = f32x8_to_bf16(acc);
         if (lane == 0) lse[(b * a.Hq + h) * a.S_q + qpos] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
 }
@@ -106,9 +108,10 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(BwdArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t h = warp; h < a.f.Hq; h += kWarps) {
         float of[8], df[8];
-        const int64_t off = (row * a.f.Hq + h) * kHeadDim + lane * 8;
-        bf16x8_to_f32(ldg16(a.o + off), of);
-        bf16x8_to_f32(ldg16(a.dout + off), df);
+        const bool dl = lane * 8 < a.f.D;
+        const int64_t off = (row * a.f.Hq + h) * a.f.D + lane * 8;
+        bf16x8_to_f32(dl ? ldg16(a.o + off) : make_uint4(0, 0, 0, 0), of);
+        bf16x8_to_f32(dl ? ldg16(a.dout + off) : make_uint4(0, 0, 0, 0), df);
         float part = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) part = fmaf(of[i], df[i], part);
@@ -129,13 +132,14 @@ __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
     const float sl2 = f.scale * kLog2e;
     const __nv_bfloat16 *kbase = f.k + b * f.ks0 + g * f.ks2 + lane * 8;
     const __nv_bfloat16 *vbase = f.v + b * f.vs0 + g * f.vs2 + lane * 8;
-    float *dkbase = kDet ? nullptr : a.dk_acc + (b * f.S_kv * f.Hkv + g) * kHeadDim + lane * 8;
-    float *dvbase = kDet ? nullptr : a.dv_acc + (b * f.S_kv * f.Hkv + g) * kHeadDim + lane * 8;
+    const bool dl = lane * 8 < f.D;
+    float *dkbase = kDet ? nullptr : a.dk_acc + (b * f.S_kv * f.Hkv + g) * f.D + lane * 8;
+    float *dvbase = kDet ? nullptr : a.dv_acc + (b * f.S_kv * f.Hkv + g) * f.D + lane * 8;
     for (int64_t hl = warp; hl < f.G; hl += kWarps) {
         const int64_t h = g * f.G + hl;
         float qf[8], df[8], dq[8];
-        bf16x8_to_f32(ldg16(f.q + b * f.qs0 + qpos * f.qs1 + h * f.qs2 + lane * 8), qf);
-        bf16x8_to_f32(ldg16(a.dout + (row * f.Hq + h) * kHeadDim + lane * 8), df);
+        bf16x8_to_f32(dl ? ldg16(f.q + b * f.qs0 + qpos * f.qs1 + h * f.qs2 + lane * 8) : make_uint4(0, 0, 0, 0), qf);
+        bf16x8_to_f32(dl ? ldg16(a.dout + (row * f.Hq + h) * f.D + lane * 8) : make_uint4(0, 0, 0, 0), df);
 #pragma unroll
         for (int i = 0; i < 8; ++i) dq[i] = 0.f;
         const float lse2 = n > 0 ? a.lse[(b * f.Hq + h) * f.S_q + qpos] * kLog2e : 0.f;
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
                     j[u] = -1;
                 }
                 float ps = 0.f, pd = 0.f;
-                if (j[u] >= 0) {
+                if (j[u] >= 0 && dl) {
                     float vf[8];
                     bf16x8_to_f32(ldg16(kbase + j[u] * f.ks1), kf[u]);
                     bf16x8_to_f32(ldg16(vbase + j[u] * f.vs1), vf);
@@ -183,16 +187,17 @@ __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) dq[i] = fmaf(ds, kf[u][i], dq[i]);
                 const float c = f.scale * ds;
+                if (!dl) continue;
                 if (kDet) {
-                    const int64_t e0 = ((b * f.S_kv + j[u]) * f.Hkv + g) * kHeadDim + lane * 8;
+                    const int64_t e0 = ((b * f.S_kv + j[u]) * f.Hkv + g) * f.D + lane * 8;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         red_add_fx(a.dk_fx, e0 + i, c * qf[i]);
                         red_add_fx(a.dv_fx, e0 + i, p * df[i]);
                     }
                 } else {
-                    float *dkj = dkbase + j[u] * f.Hkv * kHeadDim;
-                    float *dvj = dvbase + j[u] * f.Hkv * kHeadDim;
+                    float *dkj = dkbase + j[u] * f.Hkv * f.D;
+                    float *dvj = dvbase + j[u] * f.Hkv * f.D;
                     red_add_v4(dkj, c * qf[0], c * qf[1], c * qf[2], c * qf[3]);
                     red_add_v4(dkj + 4, c * qf[4], c * qf[5], c * qf[6], c * qf[7]);
                     red_add_v4(dvj, p * df[0], p * df[1], p * df[2], p * df[3]);
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_bwd_kernel(BwdArgs a) {
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) dq[i] *= f.scale;
-        *reinterpret_cast<uint4 *>(a.dq + (row * f.Hq + h) * kHeadDim + lane * 8) = f32x8_to_bf16(dq);
+        if (dl) *reinterpret_cast<uint4 *>(a.dq + (row * f.Hq + h) * f.D + lane * 8) = f32x8_to_bf16(dq);
     }
 }
 
@@ -264,7 +269,7 @@ cudaError_t launch_rowwise_backward(const BwdArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_convert_dkdv(const BwdArgs &a, cudaStream_t s) {
-    const int64_t n8 = a.f.B * a.f.S_kv * a.f.Hkv * kHeadDim / 8;
+    const int64_t n8 = a.f.B * a.f.S_kv * a.f.Hkv * a.f.D / 8;
     int64_t nb = (n8 + 255) / 256;
     int blocks = (int)(nb < 152 * 16 ? nb : 152 * 16);
     if (a.dk_fx.est)

@@ -31,6 +31,9 @@ Route recipes (each ID list is built in "generation order": the query's own
   distinct earlier blocks, in global coordinates, keeping IDs <= p.
 * ``train-step`` -- B1 S32768 Hq32 Hkv4, int32 K=2048.  Block j plus min(47, j)
   distinct earlier blocks, IDs <= q, truncated to the first 2048 IDs.
+* ``right-padded-d128`` (D = 128) and ``right-padded-mha`` (Hq = Hkv = 16):
+  variants off the pages' D = 256, G = 8 shapes, with the right-padded-blocks
+  route recipe.
 
 Random numbers: ``numpy.random.Generator(PCG64(20261202 + index))``; routes are
 drawn first, then Q, K, V and dO, each ``standard_normal(float32)`` rounded to
@@ -80,6 +83,11 @@ WORKLOADS = (
              "B1 S_q32768 S_kv131072 Hq16 Hkv2 D256, int64 K=2048, global offset 98304"),
     Workload(4, "train-step", 1, 32768, 32768, 32, 4, 256, 2048, np.int32, 1.0 / 16,
              "B1 S32768 Hq32 Hkv4 D256, int32 K=2048, 48 causal blocks clipped to 2048 IDs"),
+    # Variants beyond the pages' D = 256, G = 8 (warp-level kernels); routes as right-padded-blocks.
+    Workload(5, "right-padded-d128", 2, 4096, 4096, 16, 2, 128, 2048, np.int32, 1.0 / 128 ** 0.5,
+             "B2 S4096 Hq16 Hkv2 D128, routes as right-padded-blocks"),
+    Workload(6, "right-padded-mha", 2, 4096, 4096, 16, 16, 256, 2048, np.int32, 1.0 / 16,
+             "B2 S4096 Hq16 Hkv16 (G=1) D256, routes as right-padded-blocks"),
 )
 
 _ROWS_PER_PIECE = 2048
@@ -237,7 +245,7 @@ def make_routes(w: Workload, rng: np.random.Generator) -> np.ndarray:
         draws = _distinct_draws(rng, np.where(live, q + 1, 0), K)
         r = _noise(rng, _compact(draws), 0.05, 0.02, w.S_kv, 2**31 - 1)
         return r.reshape(1, S, K).astype(w.route_dtype)
-    if w.index == 1:
+    if w.index in (1, 5, 6):
         out = np.empty((B, S, K), np.int64)
         for b in range(B):
             pos = np.arange(S)

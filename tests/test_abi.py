@@ -79,7 +79,10 @@ def good_problem(**kw):
     ({"softmax_scale": math.inf}, 1),
     ({"softmax_scale": math.nan}, 1),
     ({"route_bits": 16}, 1),
-    ({"D": 128}, 2),
+    ({"D": 128, "q_stride": (100 * 16 * 128, 16 * 128, 128, 1), "k_stride": (300 * 2 * 128, 2 * 128, 128, 1),
+      "v_stride": (300 * 2 * 128, 2 * 128, 128, 1)}, 0),
+    ({"D": 96}, 2),
+    ({"D": 512}, 2),
     ({"S_kv": 2**31}, 2),
     ({"K": 16385}, 2),
     ({"q_stride": (100 * 16 * 256, 16 * 256, 256, 2)}, 2),

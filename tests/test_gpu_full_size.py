@@ -1,4 +1,4 @@
-"""Full-size parity on the five workloads, run through the same C-ABI calls the
+"""Full-size parity on the five workloads (and the D = 128 / G = 1 variants), run through the same C-ABI calls the
 benchmark times.  The oracle cannot redo a full step of the large workloads in
 seconds, so:
 
@@ -50,7 +50,7 @@ def _sample_keys(rng, ids_b, counts_b, S_kv, n, max_rows=1500):
     return keys, unused
 
 
-@pytest.mark.parametrize("index", [1, 2, 3, 4])
+@pytest.mark.parametrize("index", [1, 2, 3, 4, 5, 6])
 def test_workload_full_size(index):
     case = W.make_case(index)
     w = case.workload

@@ -45,12 +45,12 @@ def test_tiny_causal_rows_workload():
     assert np.all(out["o"][0, 240:] == 0) and np.all(out["dq"][0, 240:] == 0)
 
 
-def _random_case(seed, B, S_q, S_kv, Hq, Hkv, K, pattern="random", dtype=np.int32, p_empty=0.1):
+def _random_case(seed, B, S_q, S_kv, Hq, Hkv, K, pattern="random", dtype=np.int32, p_empty=0.1, D=256):
     rng = np.random.default_rng(seed)
-    q = W.bf16_normal(rng, (B, S_q, Hq, 256))
-    k = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
-    v = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
-    do = W.bf16_normal(rng, (B, S_q, Hq, 256))
+    q = W.bf16_normal(rng, (B, S_q, Hq, D))
+    k = W.bf16_normal(rng, (B, S_kv, Hkv, D))
+    v = W.bf16_normal(rng, (B, S_kv, Hkv, D))
+    do = W.bf16_normal(rng, (B, S_q, Hq, D))
     if pattern == "random":
         routes = rng.integers(-2, S_kv + 2, size=(B, S_q, K)).astype(np.int64)
     elif pattern == "blocks":
@@ -83,6 +83,30 @@ def _random_case(seed, B, S_q, S_kv, Hq, Hkv, K, pattern="random", dtype=np.int3
 def test_small_shapes(B, S_q, S_kv, Hq, Hkv, K, pattern, dtype):
     q, k, v, do, routes = _random_case(B * 7 + S_q + K, B, S_q, S_kv, Hq, Hkv, K, pattern, dtype)
     _full_compare(q, k, v, do, routes, 1.0 / 16, S_kv)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,det", [
+    (128, 16, 2, False),  # G = 8 at D = 128: the warp-level path
+    (64, 8, 8, False),    # G = 1 (MHA-shaped) at D = 64
+    (128, 6, 2, True),    # G = 3, deterministic backward
+])
+def test_other_head_dims(D, Hq, Hkv, det):
+    """Head dims 64 and 128 (the pages fix 256; these run on the warp-level path)."""
+    B, S_q, S_kv, K = 2, 60, 150, 40
+    q, k, v, do, routes = _random_case(D + Hq, B, S_q, S_kv, Hq, Hkv, K, D=D)
+    scale = 1.0 / np.sqrt(D)
+    out = run_library(q, k, v, do, routes, scale, fp32_dkdv=True, deterministic=det)
+    ids_ref, counts_ref = oracle.route_sets(routes, S_kv)
+    assert np.array_equal(out["ids"], ids_ref)
+    qd, kd, vd, dod = f64(q), f64(k), f64(v), f64(do)
+    o_ref, lse_ref = oracle.forward(qd, kd, vd, routes, scale)
+    dq_ref, dk_ref, dv_ref = oracle.backward(qd, kd, vd, routes, dod, scale)
+    assert_close("O", out["o"], o_ref)
+    assert_lse_close(out["lse"], lse_ref)
+    assert_close("dQ", out["dq"], dq_ref)
+    assert_close("dK", out["dk"], dk_ref)
+    assert_close("dV", out["dv"], dv_ref)
+    assert_close("dK fp32", out["dk32"], dk_ref)
 
 
 def test_maximum_route_slots():
@@ -156,7 +180,7 @@ def test_invalid_arguments_raise():
     with pytest.raises(qsa.QSAError, match="UNSUPPORTED"):
         qsa.qsa_attention(q.float(), k, k, r)
     with pytest.raises(qsa.QSAError, match="UNSUPPORTED"):
-        qsa.qsa_attention(q[..., :128], k[..., :128], k[..., :128], r)
+        qsa.qsa_attention(q[..., :96], k[..., :96], k[..., :96], r)  # head dim 96
     with pytest.raises(qsa.QSAError, match="INVALID"):
         qsa.qsa_attention(q, k, k[:, :4], r)
 
