@@ -16,8 +16,10 @@
 // epilogue thread turns its block's 128 columns into 128 / H scores.
 //
 //   warp 0 (producer)  loads the item's Q tile (4-D TMA, box {64, H, n_q, 1})
-//                      and the K tiles (3-D TMA, box {64, 128, 1}) into a
-//                      four-stage ring, all 128-byte swizzled;
+//                      into one of two Q buffers (the next item's loads while
+//                      this one computes) and the K tiles (3-D TMA, box
+//                      {64, 128, 1}) into a three-stage ring, all 128-byte
+//                      swizzled;
 //   warp 1 (MMA)       one thread issues the MMAs into two TMEM accumulators
 //                      (256 columns each) alternately;
 //   warps 2-9          read an accumulator (warp w: TMEM lanes 32 (w % 4) ..,
@@ -31,18 +33,23 @@
 // QSA_ERR_TIMEOUT in the status word, the roles wind down, the tensor pipe and
 // the copies drain, and the TMEM is freed.
 //
-// Selection.  One CTA per query row.  Each thread loads a contiguous segment
-// of 32 visible scores as order-preserving 32-bit keys into registers (rows
-// of up to 8192 visible blocks stay resident; longer rows are walked in
-// chunks of 8192, re-read from L2 for each pass).  A three-pass radix select
-// with 11-bit digits (shared-memory histograms, conflict-free scans) finds the
-// key T of the floor(budget / c)-th best block and how many blocks equal to T
-// to keep (lowest indices first); one block-wide scan of the per-segment
-// counts then gives every thread the output position of its first chosen
-// block, and a bit mask of its chosen keys is walked in index order, so the
-// chosen blocks come out ascending.  Each expands to its c token IDs, the
-// incomplete causal tail follows, then -1; the row is assembled in shared
-// memory and written with coalesced stores.
+// Selection.  One CTA per query row.  The row's visible scores are loaded with
+// coalesced loads as order-preserving 32-bit keys (raw bits on the product
+// path, whose scores are never negative) and transposed through shared memory
+// so that each thread holds a contiguous segment of 32 keys in registers (rows
+// of up to 8192 visible blocks; longer rows are walked in chunks of 8192,
+// re-read from L2 for each pass).  A three-pass radix select with 11-bit
+// digits finds the key T of the floor(budget / c)-th best block and how many
+// blocks equal to T to keep (lowest indices first): the first pass histograms
+// every key, then the keys of its chosen bin are gathered into shared memory
+// in index order (when they fit) and the other two passes read only those.
+// Blocks in better first-pass bins are all chosen and only the gathered keys
+// are compared with T; one block-wide scan of the per-thread counts gives
+// every thread the output position of its first chosen block, and a bit mask
+// of its chosen keys is walked in index order, so the chosen blocks come out
+// ascending.  Each expands to its c token IDs, the incomplete causal tail
+// follows, then -1; the row is assembled in shared memory and written with
+// coalesced stores.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
