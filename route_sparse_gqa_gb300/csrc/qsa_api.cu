@@ -64,8 +64,9 @@ qsa_status validate(const qsa_problem *p) {
 Layout make_layout(const qsa_problem *p) {
     Layout L{};
     L.G = p->Hq / p->Hkv;
-    // The tile path covers D = 256 and power-of-two groups of 4..64 heads; the rest runs warp-level.
-    L.T = (p->D == kHeadDim && is_pow2(L.G) && L.G >= 4 && L.G <= kTileRows) ? kTileRows / L.G : 0;
+    // The tile path covers power-of-two groups of 4..64 heads (forward: D = 256 or 128; backward:
+    // D = 256); the rest runs warp-level.
+    L.T = ((p->D == kHeadDim || p->D == 128) && is_pow2(L.G) && L.G >= 4 && L.G <= kTileRows) ? kTileRows / L.G : 0;
     L.n_tiles = L.T ? (p->S_q + L.T - 1) / L.T : 0;
     const int64_t union_cap = L.T ? std::min<int64_t>(L.T * p->K, p->S_kv) : 0;
     L.max_chunks = (union_cap + kChunkKeys - 1) / kChunkKeys;

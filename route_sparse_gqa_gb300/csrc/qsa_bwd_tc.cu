@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 bool tc_backward_supported() { return tc_device_ok(); }
 
 bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t) {
-    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs;
+    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs && a.D == kHeadDim;
 }
 
 cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_t s) {

@@ -63,15 +63,24 @@ using namespace ptx;
 constexpr int kStages = 3;
 constexpr int kThreads = 192;  // warps 0-3 softmax, 4 producer, 5 MMA
 constexpr int kMaxPairs = kMaxKVPairs;  // (b, g) tensor-map sets per launch
-constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;  // 32 KiB per K or V chunk
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
-constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
 constexpr uint32_t kNumBars = 5 + 5 * kStages + 2 * kQueueRing;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemSP = 384;  // S/P buffer b at kTmemSP + 64 b
+constexpr uint32_t kPanelBytes = kChunkKeys * 128;  // one 64-column (128-byte-wide) panel of a 64-key chunk
+
+// Shared-memory and TMEM layout for head dim D (256, or 128 for the same tiles
+// at half the width).  TMEM: O in columns 0..D-1 (fp32), Q in D..D+D/2-1 (bf16
+// pairs), then the two S/P buffers of 64 columns.
+template <int D>
+struct FwdLayout {
+    static constexpr int kPanels = D / 64;
+    static constexpr uint32_t kKVBytes = kChunkKeys * D * 2;  // per K or V chunk (32 KiB at D = 256)
+    static constexpr uint32_t kOffK = 0;
+    static constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
+    static constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+    static constexpr uint32_t kTmemO = 0, kTmemQ = D, kTmemSP = D + D / 2;  // S/P buffer b at kTmemSP + 64 b
+};
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
@@ -116,8 +125,9 @@ struct Bars {
     uint64_t *o_ready;          // PV(c) complete: V stage reusable, O current up to c
 };
 
+template <int D>
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
-    uint64_t *b = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + FwdLayout<D>::kOffBar);
     Bars r;
     r.q_ready = b + 0;
     r.q_free = b + 1;
@@ -133,28 +143,32 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     return r;
 }
 
-// Loads the 64 K or V rows of one chunk into a stage: four 64-row tile boxes
-// when the keys form one contiguous run, else 16 lanes x 4 tile::gather4.
+// Loads the 64 K or V rows of one chunk into a stage: one 64-row tile box per
+// 64-column panel when the keys form one contiguous run, else 16 lanes x
+// tile::gather4 per panel.
+template <int D>
 __device__ __forceinline__ void load_chunk_rows(uint32_t dst, const CUtensorMap *run_map, const CUtensorMap *rows_map,
                                                 uint64_t *bar, bool run, int first, const int4 &kk, int lane) {
     if (run) {
         if (lane == 0)
-            for (int kb = 0; kb < 4; ++kb) tma_load_2d(dst + kb * (kKVBytes / 4), run_map, bar, kb * 64, first);
+            for (int kb = 0; kb < FwdLayout<D>::kPanels; ++kb)
+                tma_load_2d(dst + kb * kPanelBytes, run_map, bar, kb * 64, first);
     } else if (lane < 16) {
-        for (int kb = 0; kb < 4; ++kb)
-            tma_gather4(dst + lane * 512 + kb * (kKVBytes / 4), rows_map, bar, kb * 64, kk.x, kk.y, kk.z, kk.w);
+        for (int kb = 0; kb < FwdLayout<D>::kPanels; ++kb)
+            tma_gather4(dst + lane * 512 + kb * kPanelBytes, rows_map, bar, kb * 64, kk.x, kk.y, kk.z, kk.w);
     }
 }
 
-// Thread r of the softmax warps copies its Q row (256 BF16) into TMEM lane r,
-// columns kTmemQ..kTmemQ+127 (column j holds elements 2j and 2j+1).  Rows past
-// S_q get zeros.
+// Thread r of the softmax warps copies its Q row (D BF16) into TMEM lane r,
+// columns kTmemQ..kTmemQ+D/2-1 (column j holds elements 2j and 2j+1).  Rows
+// past S_q get zeros.
+template <int D>
 __device__ __forceinline__ void load_q_row(const FwdParams &p, const Item &it, int qi, int hl, uint32_t trow) {
     const int64_t q = it.t * p.T + qi;
     const bool live = q < p.S_q;
     const uint4 *src = reinterpret_cast<const uint4 *>(p.q + it.b * p.qs0 + q * p.qs1 + (it.g * p.G + hl) * p.qs2);
 #pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
+    for (int blk = 0; blk < D / 64; ++blk) {
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -164,18 +178,20 @@ __device__ __forceinline__ void load_q_row(const FwdParams &p, const Item &it, i
             w[4 * i + 2] = v.z;
             w[4 * i + 3] = v.w;
         }
-        tmem_st32(trow + kTmemQ + blk * 32, w);
+        tmem_st32(trow + FwdLayout<D>::kTmemQ + blk * 32, w);
     }
     tmem_st_wait();
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Bars bar = bars_at(smem);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
-    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + kOffMisc + 16);  // [kQueueRing]
+    const Bars bar = bars_at<D>(smem);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 8);
+    volatile int32_t *ring = reinterpret_cast<volatile int32_t *>(smem + L::kOffMisc + 16);  // [kQueueRing]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(smem);
 
@@ -235,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             if (it.nch == 0) continue;
             // Warm L2 with the item's Q tile; the softmax warps copy it into TMEM a little later.
             if (lane == 0)
-                for (int kb = 0; kb < 4; ++kb)
+                for (int kb = 0; kb < L::kPanels; ++kb)
                     tma_prefetch_4d(&p.q_map, kb * 64, (int)(it.g * p.G), (int)(it.t * p.T), (int)it.b);
             const int pair = (int)(it.b * p.n_g + (it.g - p.g0));
             const KVMaps &maps = p.kv[pair];
@@ -259,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         ok = false;
                         break;
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(bar.k_full + sk, kKVBytes);
+                    if (lane == 0) mbar_arrive_expect_tx(bar.k_full + sk, L::kKVBytes);
                     __syncwarp();
-                    load_chunk_rows(sbase + kOffK + sk * kKVBytes, &maps.k_run, &maps.k_rows, bar.k_full + sk, run,
+                    load_chunk_rows<D>(sbase + L::kOffK + sk * L::kKVBytes, &maps.k_run, &maps.k_rows, bar.k_full + sk, run,
                                     first, kk, lane);
                     __syncwarp();
                     last_k[sk] = gk;
@@ -274,9 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         ok = false;
                         break;
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(bar.v_full + sv, kKVBytes);
+                    if (lane == 0) mbar_arrive_expect_tx(bar.v_full + sv, L::kKVBytes);
                     __syncwarp();
-                    load_chunk_rows(sbase + kOffV + sv * kKVBytes, &maps.v_run, &maps.v_rows, bar.v_full + sv, run_prev,
+                    load_chunk_rows<D>(sbase + L::kOffV + sv * L::kKVBytes, &maps.v_run, &maps.v_rows, bar.v_full + sv, run_prev,
                                     first_prev, kk_prev, lane);
                     __syncwarp();
                     last_v[sv] = gv;
@@ -310,20 +326,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         // by the tensor pipe, so one wait per pair keeps that pipe fed.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(kTileRows, kChunkKeys, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(kTileRows, kHeadDim, false, true);
+            constexpr uint32_t idesc_pv = idesc_bf16(kTileRows, D, false, true);
             auto wait1 = [&](uint64_t *b, int64_t phase) {
                 return mbar_wait(b, (uint32_t)(phase & 1), abort_flag, p.wait_limit_ns);
             };
             auto issue_s = [&](int64_t g2, bool last_s) {
                 const int s = stage_of(g2), sb = (int)(g2 & 1);
-                const uint32_t ka = sbase + kOffK + s * kKVBytes;
-                const uint32_t sp = tmem + kTmemSP + sb * kChunkKeys;
+                const uint32_t ka = sbase + L::kOffK + s * L::kKVBytes;
+                const uint32_t sp = tmem + L::kTmemSP + sb * kChunkKeys;
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb) {
+                for (int kb = 0; kb < L::kPanels; ++kb) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t bd = sdesc_sw128(ka + kb * (kKVBytes / 4) + k * 32, 16, 1024);
-                        mma_bf16_ts(sp, tmem + kTmemQ + (kb * 4 + k) * 8, bd, idesc_qk, (kb | k) ? 1u : 0u);
+                        const uint64_t bd = sdesc_sw128(ka + kb * kPanelBytes + k * 32, 16, 1024);
+                        mma_bf16_ts(sp, tmem + L::kTmemQ + (kb * 4 + k) * 8, bd, idesc_qk, (kb | k) ? 1u : 0u);
                     }
                 }
                 mma_commit(bar.s_full + s);
@@ -331,12 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             };
             auto issue_pv = [&](int64_t g2, bool first) {
                 const int s = stage_of(g2), sb = (int)(g2 & 1);
-                const uint32_t va = sbase + kOffV + s * kKVBytes;
-                const uint32_t pa = tmem + kTmemSP + sb * kChunkKeys;
+                const uint32_t va = sbase + L::kOffV + s * L::kKVBytes;
+                const uint32_t pa = tmem + L::kTmemSP + sb * kChunkKeys;
 #pragma unroll
                 for (int k = 0; k < kChunkKeys / 16; ++k) {
-                    const uint64_t bd = sdesc_sw128(va + k * 2048, kKVBytes / 4, 1024);
-                    mma_bf16_ts(tmem + kTmemO, pa + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
+                    const uint64_t bd = sdesc_sw128(va + k * 2048, kPanelBytes, 1024);
+                    mma_bf16_ts(tmem + L::kTmemO, pa + k * 8, bd, idesc_pv, (first && k == 0) ? 0u : 1u);
                 }
                 mma_commit(bar.o_ready + s);
             };
@@ -393,18 +409,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             const int64_t q = it.t * p.T + qi;
             const int64_t h = it.g * p.G + hl;
             const bool live = q < p.S_q;
-            __nv_bfloat16 *orow = p.o + ((it.b * p.S_q + q) * p.Hq + h) * kHeadDim;
+            __nv_bfloat16 *orow = p.o + ((it.b * p.S_q + q) * p.Hq + h) * D;
             if (it.nch == 0) {
                 if (live) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
-                    for (int i = 0; i < kHeadDim / 8; ++i) reinterpret_cast<uint4 *>(orow)[i] = z;
+                    for (int i = 0; i < D / 8; ++i) reinterpret_cast<uint4 *>(orow)[i] = z;
                     p.lse[(it.b * p.Hq + h) * p.S_q + q] = -INFINITY;
                 }
                 ok = queue_take(ring, bar.item_full, bar.item_empty, ++pos, abort_flag, p.wait_limit_ns, true, idx);
                 continue;
             }
             if (!have_q) {  // only for the first non-empty item; later ones are loaded ahead
-                load_q_row(p, it, qi, hl, trow);
+                load_q_row<D>(p, it, qi, hl, trow);
                 tc_fence_before();
                 mbar_arrive(bar.q_ready);
             }
@@ -413,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             float m = -INFINITY, l = 0.f;
             for (int c = 0; c < it.nch; ++c, ++gc) {
                 const int sb = (int)(gc & 1), st = stage_of(gc);
-                const uint32_t sp = trow + kTmemSP + sb * kChunkKeys;
+                const uint32_t sp = trow + L::kTmemSP + sb * kChunkKeys;
                 const uint64_t mask = mask_next;
                 if (c + 1 < it.nch) mask_next = __ldg(mrow + (c + 1) * p.T);
                 // V(c) and, within the item, K(c+2) must have landed before P(c) is released: the MMA thread
@@ -457,13 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     tc_fence_after();
                     const float alpha = need ? ex2(m - mx) : 1.f;
 #pragma unroll 1
-                    for (int blk = 0; blk < kHeadDim / 32; ++blk) {
+                    for (int blk = 0; blk < D / 32; ++blk) {
                         uint32_t o[32];
-                        tmem_ld32(trow + kTmemO + blk * 32, o);
+                        tmem_ld32(trow + L::kTmemO + blk * 32, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        tmem_st32(trow + kTmemO + blk * 32, o);
+                        tmem_st32(trow + L::kTmemO + blk * 32, o);
                     }
                     tmem_st_wait();
                     if (need) {
@@ -508,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    load_q_row(p, nx, qi, hl, trow);
+                    load_q_row<D>(p, nx, qi, hl, trow);
                     tc_fence_before();
                     mbar_arrive(bar.q_ready);
                     have_q = true;
@@ -522,9 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int blk = 0; blk < kHeadDim / 32; ++blk) {
+            for (int blk = 0; blk < D / 32; ++blk) {
                 uint32_t o[32];
-                tmem_ld32(trow + kTmemO + blk * 32, o);
+                tmem_ld32(trow + L::kTmemO + blk * 32, o);
                 tmem_ld_wait();
                 if (live) {
 #pragma unroll
@@ -557,19 +573,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 bool tc_forward_supported() { return tc_device_ok(); }
 
 bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t) {
-    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs;
+    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs && (a.D == 256 || a.D == 128);
 }
+
+namespace {
+template <int D>
+cudaError_t set_fwd_smem() {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             FwdLayout<D>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    return cudaSuccess;
+}
+}  // namespace
 
 cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s) {
     FwdParams p;
     memset(&p, 0, sizeof(p));
-    if (!tc_encode_tile_map(&p.q_map, a.q, a.Hq, a.S_q, a.B, a.qs2, a.qs1, a.qs0, a.G, t.T))
+    if (!tc_encode_tile_map(&p.q_map, a.q, a.Hq, a.S_q, a.B, a.qs2, a.qs1, a.qs0, a.G, t.T, a.D))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    {
+        cudaError_t e = a.D == 128 ? set_fwd_smem<128>() : set_fwd_smem<256>();
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     const int sms = tc_num_sms();
     const int64_t g_per_launch = std::max<int64_t>(1, kMaxPairs / a.B);
@@ -604,7 +632,10 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
             for (int64_t gi = 0; gi < n_g; ++gi)
                 if (!tc_encode_kv_maps(&p.kv[b * n_g + gi], a, b, g0 + gi)) return cudaErrorInvalidValue;
         const int grid = (int)std::min<int64_t>(p.n_items, sms);
-        tc_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+        if (a.D == 128)
+            tc_fwd_kernel<128><<<grid, kThreads, FwdLayout<128>::kSmemBytes, s>>>(p);
+        else
+            tc_fwd_kernel<256><<<grid, kThreads, FwdLayout<256>::kSmemBytes, s>>>(p);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -26,12 +26,14 @@ int tc_num_sms();
 // variable QSA_DEBUG_WAIT_LIMIT_NS sets it (a test hook that makes a wait run
 // out on purpose; the kernels then report QSA_ERR_TIMEOUT and wind down).
 uint64_t tc_wait_limit_ns(uint64_t fallback);
-// 2-D map over `rows` rows of 256 bf16 (row pitch in elements), box 64 x 1,
+// 2-D map over `rows` rows of D bf16 (row pitch in elements), box 64 x 1,
 // 128-byte swizzle: the operand of tile::gather4 row gathers.
-bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems);
+bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems,
+                        int64_t D = kHeadDim);
 // Same tensor with a 64 x 64 box: one tile load brings 64 consecutive rows
 // (a contiguous run of keys) in the layout the 64-row gathers produce.
-bool tc_encode_run_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems);
+bool tc_encode_run_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems,
+                       int64_t D = kHeadDim);
 
 // Tensor maps of one (batch, KV head) pair: K and V for row gathers and for
 // 64-row contiguous runs.
@@ -40,10 +42,10 @@ struct KVMaps {
 };
 constexpr int kMaxKVPairs = 32;  // pairs per launch (kernel parameter space)
 bool tc_encode_kv_maps(KVMaps *m, const AttnArgs &a, int64_t b, int64_t g);
-// 4-D map over a [B, S, H, 256] bf16 tensor (strides in elements), box
+// 4-D map over a [B, S, H, D] bf16 tensor (strides in elements), box
 // {64, G, T, 1}, 128-byte swizzle: one (T queries x G heads) tile per 64 columns.
 bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, int64_t B, int64_t sH, int64_t sS,
-                        int64_t sB, int64_t G, int64_t T);
+                        int64_t sB, int64_t G, int64_t T, int64_t D = kHeadDim);
 
 // Generic BF16 tensor map, 128-byte swizzle, zero fill out of bounds: dims[0]
 // is the innermost (unit-stride) extent, strides[i] (elements) the pitch of

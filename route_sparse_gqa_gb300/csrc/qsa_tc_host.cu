@@ -50,8 +50,8 @@ uint64_t tc_wait_limit_ns(uint64_t fallback) {
     return (end && *end == '\0') ? (uint64_t)v : fallback;
 }
 
-bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems) {
-    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems, int64_t D) {
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 2};
     const cuuint32_t box[2] = {64, 1};
     const cuuint32_t estr[2] = {1, 1};
@@ -60,8 +60,8 @@ bool tc_encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t 
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool tc_encode_run_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems) {
-    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+bool tc_encode_run_map(CUtensorMap *m, const void *base, int64_t rows, int64_t row_stride_elems, int64_t D) {
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)row_stride_elems * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)kChunkKeys};
     const cuuint32_t estr[2] = {1, 1};
@@ -72,13 +72,14 @@ bool tc_encode_run_map(CUtensorMap *m, const void *base, int64_t rows, int64_t r
 
 bool tc_encode_kv_maps(KVMaps *m, const AttnArgs &a, int64_t b, int64_t g) {
     const __nv_bfloat16 *kb = a.k + b * a.ks0 + g * a.ks2, *vb = a.v + b * a.vs0 + g * a.vs2;
-    return tc_encode_rows_map(&m->k_rows, kb, a.S_kv, a.ks1) && tc_encode_rows_map(&m->v_rows, vb, a.S_kv, a.vs1) &&
-           tc_encode_run_map(&m->k_run, kb, a.S_kv, a.ks1) && tc_encode_run_map(&m->v_run, vb, a.S_kv, a.vs1);
+    return tc_encode_rows_map(&m->k_rows, kb, a.S_kv, a.ks1, a.D) &&
+           tc_encode_rows_map(&m->v_rows, vb, a.S_kv, a.vs1, a.D) && tc_encode_run_map(&m->k_run, kb, a.S_kv, a.ks1, a.D) &&
+           tc_encode_run_map(&m->v_run, vb, a.S_kv, a.vs1, a.D);
 }
 
 bool tc_encode_tile_map(CUtensorMap *m, const void *base, int64_t H, int64_t S, int64_t B, int64_t sH, int64_t sS,
-                        int64_t sB, int64_t G, int64_t T) {
-    const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+                        int64_t sB, int64_t G, int64_t T, int64_t D) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)sH * 2, (cuuint64_t)sS * 2, (cuuint64_t)sB * 2};
     const cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)T, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
