@@ -7,7 +7,7 @@ unbuilt library raise.
 
 The call signature follows ``flex_sparse_gqa_attention`` /
 ``fa4_sparse_gqa_attention`` on the NeMo-AutoModel Qwen3.8-Flash-Next pages:
-``query [B,S_q,Hq,D]``, ``key``/``value [B,S_kv,Hkv,D]`` (BF16, D = 256; 64 and 128 on the warp-level kernels),
+``query [B,S_q,Hq,D]``, ``key``/``value [B,S_kv,Hkv,D]`` (BF16, D = 256; also 128, and 64 on the warp-level kernels),
 ``selected_token_ids [B,S_q,K]`` signed int32/int64 in K/V coordinates (-1 and
 out-of-range IDs are padding, duplicates count once), ``softmax_scale``
 defaulting to ``1/sqrt(D)``.  The output is an independent BF16 tensor.

@@ -8,10 +8,11 @@
 //   producer warp  gathers V then K rows (TMA tile::gather4) once the previous
 //                  chunk's MMAs have released them (single stage each; V is
 //                  free early, after the dP MMA);
-//   MMA warp       S = Q K^T and dP = dO V^T (M128 N64 K256) into TMEM;
-//                  after the softmax: dQ += dS K (M128 N256 K64, TMEM
+//   MMA warp       S = Q K^T and dP = dO V^T (M128 N64 K=D) into TMEM;
+//                  after the softmax: dQ += dS K (M128 N=D K64, TMEM
 //                  accumulator over all chunks of the item), then for each
-//                  half of D: dK^T = Q^T dS and dV^T = dO^T P (M128 N64 K128,
+//                  128-row half of D (one at D = 128): dK^T = Q^T dS and
+//                  dV^T = dO^T P (M128 N64 K128,
 //                  both operands MN-major straight from the Q/dO tiles and the
 //                  P/dS buffers) into TMEM;
 //   softmax warps  thread = row: P = mask ? exp2(s*scale*log2e - LSE*log2e) : 0,
@@ -25,8 +26,8 @@
 //
 // So each gathered K/V row and each (key, d) accumulator update serves every
 // head of the group and every tile query that routes to that key, instead of
-// once per (query, head).  TMEM (512 columns): dQ 0-255, S 256-319,
-// dP 320-383, dK^T 384-447, dV^T 448-511.  All waits are bounded (2 s); a
+// once per (query, head).  Head dim D = 256 or 128.  TMEM (512 columns): dQ
+// 0..D-1, S 256-319, dP 320-383, dK^T 384-447, dV^T 448-511.  All waits are bounded (2 s); a
 // timeout is recorded in the status word, the roles wind down, in-flight
 // copies and MMAs are drained, and the TMEM is freed.
 #include <algorithm>
@@ -44,21 +45,33 @@ using namespace ptx;
 
 constexpr int kThreads = 320;  // warps 0-3 softmax, 4-7 flush, 8 producer, 9 MMA
 constexpr int kMaxPairs = kMaxKVPairs;
-constexpr uint32_t kTileBytes = kTileRows * kHeadDim * 2;    // 64 KiB (Q or dO tile)
-constexpr uint32_t kKVBytes = kChunkKeys * kHeadDim * 2;     // 32 KiB
 constexpr uint32_t kPBytes = kTileRows * kChunkKeys * 2;     // 16 KiB
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffDO = kOffQ + kTileBytes;
-constexpr uint32_t kOffK = kOffDO + kTileBytes;
-constexpr uint32_t kOffV = kOffK + kKVBytes;
-constexpr uint32_t kOffP = kOffV + kKVBytes;
-constexpr uint32_t kOffDS = kOffP + kPBytes;
-constexpr uint32_t kOffBar = kOffDS + kPBytes;
+// The Q/dO tiles and the K/V chunks sit in shared memory as 64-column panels
+// (128-byte swizzle), so the panel strides do not depend on the head dim.
+constexpr uint32_t kTilePanel = kTileRows * 128;  // 16 KiB: 64 columns of a 128-row tile
+constexpr uint32_t kKVPanel = kChunkKeys * 128;   // 8 KiB: 64 columns of a 64-key chunk
 constexpr uint32_t kBarItemFull = 16;  // work queue ring: full [kQueueRing], then empty [kQueueRing]
 constexpr uint32_t kBarItemEmpty = kBarItemFull + kQueueRing;
 constexpr uint32_t kNumBars = kBarItemEmpty + kQueueRing;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
+
+// Shared-memory layout for head dim D (256, or 128 with the same tiles at half
+// the width: 128 KiB instead of 224 KiB).
+template <int D>
+struct BwdLayout {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kHalves = D / 128;  // dK^T / dV^T MMAs cover 128 head-dim rows each
+    static constexpr uint32_t kTileBytes = kTileRows * D * 2;  // Q or dO tile (64 KiB at D = 256)
+    static constexpr uint32_t kKVBytes = kChunkKeys * D * 2;   // K or V chunk (32 KiB at D = 256)
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffDO = kOffQ + kTileBytes;
+    static constexpr uint32_t kOffK = kOffDO + kTileBytes;
+    static constexpr uint32_t kOffV = kOffK + kKVBytes;
+    static constexpr uint32_t kOffP = kOffV + kKVBytes;
+    static constexpr uint32_t kOffDS = kOffP + kPBytes;
+    static constexpr uint32_t kOffBar = kOffDS + kPBytes;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemDQ = 0, kTmemS = 256, kTmemDP = 320, kTmemDKT = 384, kTmemDVT = 448;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -93,9 +106,14 @@ enum BarId {
     kDQReady, kDQFree, kDrain, kSFull
 };
 
-// kDet: the flush adds dK/dV into the exact accumulators (FxAcc: bitwise reproducible sums).
-template <bool kDet>
+// D: head dim (128 or 256).  kDet: the flush adds dK/dV into the exact accumulators (FxAcc: bitwise
+// reproducible sums).
+template <int D, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
+    using L = BwdLayout<D>;
+    constexpr uint32_t kOffQ = L::kOffQ, kOffDO = L::kOffDO, kOffK = L::kOffK, kOffV = L::kOffV;
+    constexpr uint32_t kOffP = L::kOffP, kOffDS = L::kOffDS, kOffBar = L::kOffBar, kOffMisc = L::kOffMisc;
+    constexpr uint32_t kTileBytes = L::kTileBytes, kKVBytes = L::kKVBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
@@ -157,10 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             }
             if (lane == 0) {
                 mbar_arrive_expect_tx(bars + kQFull, 2 * kTileBytes);
-                for (int kb = 0; kb < 4; ++kb) {
-                    tma_load_4d(sbase + kOffQ + kb * (kTileBytes / 4), &p.q_map, bars + kQFull, kb * 64,
+                for (int kb = 0; kb < L::kPanels; ++kb) {
+                    tma_load_4d(sbase + kOffQ + kb * kTilePanel, &p.q_map, bars + kQFull, kb * 64,
                                 (int)(it.g * p.G), (int)(it.t * p.T), (int)it.b);
-                    tma_load_4d(sbase + kOffDO + kb * (kTileBytes / 4), &p.do_map, bars + kQFull, kb * 64,
+                    tma_load_4d(sbase + kOffDO + kb * kTilePanel, &p.do_map, bars + kQFull, kb * 64,
                                 (int)(it.g * p.G), (int)(it.t * p.T), (int)it.b);
                 }
             }
@@ -183,11 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 __syncwarp();
                 if (run) {
                     if (lane == 0)
-                        for (int kb = 0; kb < 4; ++kb)
-                            tma_load_2d(sbase + kOffV + kb * (kKVBytes / 4), &maps.v_run, bars + kKFull, kb * 64, first);
+                        for (int kb = 0; kb < L::kPanels; ++kb)
+                            tma_load_2d(sbase + kOffV + kb * kKVPanel, &maps.v_run, bars + kKFull, kb * 64, first);
                 } else if (lane < 16) {
-                    for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(sbase + kOffV + lane * 512 + kb * (kKVBytes / 4), &maps.v_rows, bars + kKFull,
+                    for (int kb = 0; kb < L::kPanels; ++kb)
+                        tma_gather4(sbase + kOffV + lane * 512 + kb * kKVPanel, &maps.v_rows, bars + kKFull,
                                     kb * 64, kk.x, kk.y, kk.z, kk.w);
                 }
                 __syncwarp();
@@ -199,11 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 __syncwarp();
                 if (run) {
                     if (lane == 0)
-                        for (int kb = 0; kb < 4; ++kb)
-                            tma_load_2d(sbase + kOffK + kb * (kKVBytes / 4), &maps.k_run, bars + kKFull, kb * 64, first);
+                        for (int kb = 0; kb < L::kPanels; ++kb)
+                            tma_load_2d(sbase + kOffK + kb * kKVPanel, &maps.k_run, bars + kKFull, kb * 64, first);
                 } else if (lane < 16) {
-                    for (int kb = 0; kb < 4; ++kb)
-                        tma_gather4(sbase + kOffK + lane * 512 + kb * (kKVBytes / 4), &maps.k_rows, bars + kKFull,
+                    for (int kb = 0; kb < L::kPanels; ++kb)
+                        tma_gather4(sbase + kOffK + lane * 512 + kb * kKVPanel, &maps.k_rows, bars + kKFull,
                                     kb * 64, kk.x, kk.y, kk.z, kk.w);
                 }
                 __syncwarp();
@@ -226,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     } else if (warp == 9) {
         // ---------------- MMA issuer ----------------
         constexpr uint32_t idesc_n64 = idesc_bf16(kTileRows, kChunkKeys, false, false);   // S, dP
-        constexpr uint32_t idesc_dq = idesc_bf16(kTileRows, kHeadDim, false, true);       // dQ += dS K
+        constexpr uint32_t idesc_dq = idesc_bf16(kTileRows, D, false, true);       // dQ += dS K
         constexpr uint32_t idesc_t = idesc_bf16(kTileRows, kChunkKeys, true, true);       // dK^T, dV^T
         int64_t gc = 0, qc = 0, u = 0;
         Item it;
@@ -251,20 +269,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 if (lane == 0) {
                     // S first (its own completion barrier), then dP.
 #pragma unroll
-                    for (int kb = 0; kb < 4; ++kb) {
+                    for (int kb = 0; kb < L::kPanels; ++kb) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            mma_bf16(tmem + kTmemS, sdesc_sw128(sbase + kOffQ + kb * (kTileBytes / 4) + k * 32, 16, 1024),
-                                     sdesc_sw128(sbase + kOffK + kb * (kKVBytes / 4) + k * 32, 16, 1024), idesc_n64,
+                            mma_bf16(tmem + kTmemS, sdesc_sw128(sbase + kOffQ + kb * kTilePanel + k * 32, 16, 1024),
+                                     sdesc_sw128(sbase + kOffK + kb * kKVPanel + k * 32, 16, 1024), idesc_n64,
                                      (kb | k) ? 1u : 0u);
                     }
                     mma_commit(bars + kSFull);
 #pragma unroll
-                    for (int kb = 0; kb < 4; ++kb) {
+                    for (int kb = 0; kb < L::kPanels; ++kb) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            mma_bf16(tmem + kTmemDP, sdesc_sw128(sbase + kOffDO + kb * (kTileBytes / 4) + k * 32, 16, 1024),
-                                     sdesc_sw128(sbase + kOffV + kb * (kKVBytes / 4) + k * 32, 16, 1024), idesc_n64,
+                            mma_bf16(tmem + kTmemDP, sdesc_sw128(sbase + kOffDO + kb * kTilePanel + k * 32, 16, 1024),
+                                     sdesc_sw128(sbase + kOffV + kb * kKVPanel + k * 32, 16, 1024), idesc_n64,
                                      (kb | k) ? 1u : 0u);
                     }
                     mma_commit(bars + kSDFull);
@@ -280,13 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
                     for (int k = 0; k < kChunkKeys / 16; ++k)
                         mma_bf16(tmem + kTmemDQ, sdesc_sw128(sbase + kOffDS + k * 32, 16, 1024),
-                                 sdesc_sw128(sbase + kOffK + k * 2048, kKVBytes / 4, 1024), idesc_dq,
+                                 sdesc_sw128(sbase + kOffK + k * 2048, kKVPanel, 1024), idesc_dq,
                                  (c == 0 && k == 0) ? 0u : 1u);
                     mma_commit(bars + kKEmpty);
                     if (c == it.nch - 1) mma_commit(bars + kDQReady);
                 }
                 __syncwarp();
-                for (int h = 0; h < 2; ++h, ++u) {
+                for (int h = 0; h < L::kHalves; ++h, ++u) {
                     if (u > 0 && !wait(kFlushDone, u - 1)) {
                         ok = false;
                         break;
@@ -295,10 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                            const uint32_t aoff = (2 * h) * (kTileBytes / 4) + kk * 2048;
-                            mma_bf16(tmem + kTmemDKT, sdesc_sw128(sbase + kOffQ + aoff, kTileBytes / 4, 1024),
+                            const uint32_t aoff = (2 * h) * kTilePanel + kk * 2048;
+                            mma_bf16(tmem + kTmemDKT, sdesc_sw128(sbase + kOffQ + aoff, kTilePanel, 1024),
                                      sdesc_sw128(sbase + kOffDS + kk * 2048, kPBytes, 1024), idesc_t, kk ? 1u : 0u);
-                            mma_bf16(tmem + kTmemDVT, sdesc_sw128(sbase + kOffDO + aoff, kTileBytes / 4, 1024),
+                            mma_bf16(tmem + kTmemDVT, sdesc_sw128(sbase + kOffDO + aoff, kTilePanel, 1024),
                                      sdesc_sw128(sbase + kOffP + kk * 2048, kPBytes, 1024), idesc_t, kk ? 1u : 0u);
                         }
                         mma_commit(bars + kGradsFull);
@@ -336,11 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             const int64_t q = it.t * p.T + qi;
             const int64_t h = it.g * p.G + hl;
             const bool live = q < p.S_q;
-            __nv_bfloat16 *dqrow = p.dq + ((it.b * p.S_q + q) * p.Hq + h) * kHeadDim;
+            __nv_bfloat16 *dqrow = p.dq + ((it.b * p.S_q + q) * p.Hq + h) * D;
             if (it.nch == 0) {
                 if (live) {
                     const uint4 z = make_uint4(0, 0, 0, 0);
-                    for (int i = 0; i < kHeadDim / 8; ++i) reinterpret_cast<uint4 *>(dqrow)[i] = z;
+                    for (int i = 0; i < D / 8; ++i) reinterpret_cast<uint4 *>(dqrow)[i] = z;
                 }
                 continue;
             }
@@ -416,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             }
             tc_fence_after();
 #pragma unroll 1
-            for (int blk = 0; blk < kHeadDim / 32; ++blk) {
+            for (int blk = 0; blk < D / 32; ++blk) {
                 uint32_t o[32];
                 tmem_ld32(trow + kTmemDQ + blk * 32, o);
                 tmem_ld_wait();
@@ -448,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             if (!ok || idx < 0) break;
             queue_decode(p, idx, it);
             if (it.nch == 0) continue;
-            const int64_t row_stride = p.Hkv * kHeadDim;
-            const int64_t base_off = (it.b * p.S_kv * p.Hkv + it.g) * kHeadDim + quarter * 32 + lane;
+            const int64_t row_stride = p.Hkv * D;
+            const int64_t base_off = (it.b * p.S_kv * p.Hkv + it.g) * D + quarter * 32 + lane;
             float *dk_base = kDet ? p.dk_fx.est + base_off : p.dk_acc + base_off;
             float *dv_base = kDet ? p.dv_fx.est + base_off : p.dv_acc + base_off;
             uint32_t *dk_lo = kDet ? p.dk_fx.lo + base_off : nullptr;
@@ -462,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 // back to back.
                 const int32_t *keys = p.tile_keys + (it.tile * p.max_chunks + c) * kChunkKeys;
                 const int32_t key_lo = __ldg(keys + lane), key_hi = __ldg(keys + 32 + lane);
-                for (int h = 0; h < 2; ++h, ++u) {
+                for (int h = 0; h < L::kHalves; ++h, ++u) {
                     if (!wait(kGradsFull, u)) {
                         ok = false;
                         break;
@@ -503,29 +521,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 
 }  // namespace
 
+namespace {
+template <int D>
+cudaError_t set_bwd_smem() {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             BwdLayout<D>::kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(tc_bwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     BwdLayout<D>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    return cudaSuccess;
+}
+}  // namespace
+
 bool tc_backward_supported() { return tc_device_ok(); }
 
 bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t) {
-    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs && a.D == kHeadDim;
+    return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs && (a.D == 256 || a.D == 128);
 }
 
 cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_t s) {
     const AttnArgs &a = bw.f;
+    const int64_t D = a.D;
     BwdParams p;
     memset(&p, 0, sizeof(p));
-    if (!tc_encode_tile_map(&p.q_map, a.q, a.Hq, a.S_q, a.B, a.qs2, a.qs1, a.qs0, a.G, t.T))
+    if (!tc_encode_tile_map(&p.q_map, a.q, a.Hq, a.S_q, a.B, a.qs2, a.qs1, a.qs0, a.G, t.T, D))
         return cudaErrorInvalidValue;
-    if (!tc_encode_tile_map(&p.do_map, bw.dout, a.Hq, a.S_q, a.B, kHeadDim, a.Hq * kHeadDim,
-                            a.S_q * a.Hq * kHeadDim, a.G, t.T))
+    if (!tc_encode_tile_map(&p.do_map, bw.dout, a.Hq, a.S_q, a.B, D, a.Hq * D, a.S_q * a.Hq * D, a.G, t.T, D))
         return cudaErrorInvalidValue;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(tc_bwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    {
+        cudaError_t e = D == 128 ? set_bwd_smem<128>() : set_bwd_smem<256>();
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     const int sms = tc_num_sms();
     const int64_t g_per_launch = std::max<int64_t>(1, kMaxPairs / a.B);
@@ -564,10 +594,18 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
             for (int64_t gi = 0; gi < n_g; ++gi)
                 if (!tc_encode_kv_maps(&p.kv[b * n_g + gi], a, b, g0 + gi)) return cudaErrorInvalidValue;
         const int grid = (int)std::min<int64_t>(p.n_items, sms);
-        if (bw.dk_fx.est)
-            tc_bwd_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(p);
-        else
-            tc_bwd_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(p);
+        const bool det = bw.dk_fx.est != nullptr;
+        if (D == 128) {
+            if (det)
+                tc_bwd_kernel<128, true><<<grid, kThreads, BwdLayout<128>::kSmemBytes, s>>>(p);
+            else
+                tc_bwd_kernel<128, false><<<grid, kThreads, BwdLayout<128>::kSmemBytes, s>>>(p);
+        } else {
+            if (det)
+                tc_bwd_kernel<256, true><<<grid, kThreads, BwdLayout<256>::kSmemBytes, s>>>(p);
+            else
+                tc_bwd_kernel<256, false><<<grid, kThreads, BwdLayout<256>::kSmemBytes, s>>>(p);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -83,7 +83,8 @@ WORKLOADS = (
              "B1 S_q32768 S_kv131072 Hq16 Hkv2 D256, int64 K=2048, global offset 98304"),
     Workload(4, "train-step", 1, 32768, 32768, 32, 4, 256, 2048, np.int32, 1.0 / 16,
              "B1 S32768 Hq32 Hkv4 D256, int32 K=2048, 48 causal blocks clipped to 2048 IDs"),
-    # Variants beyond the pages' D = 256, G = 8 (warp-level kernels); routes as right-padded-blocks.
+    # Variants beyond the pages' D = 256, G = 8 (D = 128 on the tile kernels, G = 1 on the warp-level
+    # kernels); routes as right-padded-blocks.
     Workload(5, "right-padded-d128", 2, 4096, 4096, 16, 2, 128, 2048, np.int32, 1.0 / 128 ** 0.5,
              "B2 S4096 Hq16 Hkv2 D128, routes as right-padded-blocks"),
     Workload(6, "right-padded-mha", 2, 4096, 4096, 16, 16, 256, 2048, np.int32, 1.0 / 16,

@@ -86,12 +86,14 @@ def test_small_shapes(B, S_q, S_kv, Hq, Hkv, K, pattern, dtype):
 
 
 @pytest.mark.parametrize("D,Hq,Hkv,det", [
-    (128, 16, 2, False),  # G = 8 at D = 128: the warp-level path
-    (64, 8, 8, False),    # G = 1 (MHA-shaped) at D = 64
-    (128, 6, 2, True),    # G = 3, deterministic backward
+    (128, 16, 2, False),  # G = 8 at D = 128: the tile path
+    (128, 8, 2, True),    # G = 4 at D = 128: the tile path, deterministic backward
+    (64, 8, 8, False),    # G = 1 (MHA-shaped) at D = 64: the warp-level path
+    (128, 6, 2, True),    # G = 3: the warp-level path, deterministic backward
 ])
 def test_other_head_dims(D, Hq, Hkv, det):
-    """Head dims 64 and 128 (the pages fix 256; these run on the warp-level path)."""
+    """Head dims 64 and 128 (the pages fix 256): D = 128 with G dividing 128 on the
+    tile path, the rest on the warp-level path."""
     B, S_q, S_kv, K = 2, 60, 150, 40
     q, k, v, do, routes = _random_case(D + Hq, B, S_q, S_kv, Hq, Hkv, K, D=D)
     scale = 1.0 / np.sqrt(D)
