@@ -7,9 +7,10 @@
 //   route_rows_kernel  one CTA per query row: read the row's K route slots in
 //                      their own width (int32 or int64), keep 0 <= id < S_kv
 //                      (invalid values, huge int64 included, never reach an
-//                      index), set their bits in a shared-memory bitmap over
-//                      the row's id range and read the bitmap back in order
-//                      (sorted, repeats gone); a bitonic sort handles rows
+//                      index), mark them in a shared-memory byte map (rows
+//                      spread wider: a bitmap) over the row's id range and
+//                      read it back in order with coalesced stores (sorted,
+//                      repeats gone); a bitonic sort handles rows
 //                      whose ids are spread over a very wide range.
 //                      Output: ascending unique IDs (int32, -1 tail) + count.
 //   route_tiles_kernel one CTA per tile of T consecutive query rows: the union
@@ -32,8 +33,13 @@ constexpr int kRowThreads = 128;
 constexpr int kTileThreads = 512;
 constexpr int kTileWindow = 4096;  // keys per window of the shared-memory membership table
 constexpr int kTileBatches = 8;   // 32-id batches of one row read per step (independent loads)
-constexpr int kRowWindowBits = 65536;  // keys per window of a row's shared-memory bitmap (8 KiB)
-constexpr int kRowMaxWindows = 8;      // wider rows fall back to the bitonic sort
+constexpr int kRowMapKeys = 16384;       // rows whose ids span at most this many keys: shared-memory byte map
+constexpr int kRowWindowBits = 65536;    // wider rows: keys per window of a shared-memory bitmap (8 KiB)
+constexpr int kRowMaxWindows = 8;        // still wider rows fall back to the bitonic sort
+// Shared memory of the map and bitmap passes: byte map + its bit words + word offsets, or bitmap + offsets.
+constexpr size_t kRowSmem = kRowMapKeys + (size_t)kRowMapKeys / 32 * 8 > (size_t)kRowWindowBits / 32 * 8
+                                ? kRowMapKeys + (size_t)kRowMapKeys / 32 * 8
+                                : (size_t)kRowWindowBits / 32 * 8;
 constexpr int kRowCache = 16;          // route slots per thread kept in registers (K <= 16 * kRowThreads)
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int &total) {
@@ -70,12 +76,23 @@ __device__ __forceinline__ int64_t load_route(const RowsArgs &a, int64_t b, int6
                               : (int64_t) static_cast<const int32_t *>(a.routes)[off];
 }
 
-// Sorting by bitmap: the row's valid ids set bits in a shared-memory bitmap
-// over a window of key space; a popcount scan over the bitmap then yields the
-// ids ascending with repeats gone.  Cost O(K + range/32) per window; rows whose
-// ids span more than kRowMaxWindows windows use the bitonic sort instead.
-__global__ void __launch_bounds__(kRowThreads) route_rows_kernel(RowsArgs a, int P) {
-    extern __shared__ uint32_t rsm[];  // bitmap [kRowWindowBits/32] or bitonic buffer [P]
+// Bytes b0..b3 of w, each 0 or 1, as the bits 0..3 of a nibble: the product
+// puts byte k's value alone at bit 21 + k (the four partial products of each
+// byte land on distinct bits, so nothing carries into bits 21..24).
+__device__ __forceinline__ uint32_t flag_nibble(uint32_t w) { return ((w * 0x00204081u) >> 21) & 0xFu; }
+
+// Sorting without comparisons.  A row whose valid ids span at most kRowMapKeys
+// keys marks them in a shared-memory byte map (plain byte stores: repeated or
+// neighbouring ids need no atomics), packed afterwards into 32-key bit words.
+// Wider rows set bits of a shared-memory bitmap with atomicOr, a window of
+// kRowWindowBits keys at a time.  Either way one block scan of the words'
+// popcounts gives every word its output offset, and each warp then writes a
+// word's keys as one contiguous run (lane = bit): the ids come out ascending
+// with repeats gone, in coalesced stores.  Cost O(K + range/16) for the map,
+// O(K + range/32) per bitmap window; rows whose ids span more than
+// kRowMaxWindows windows use the bitonic sort instead.
+__global__ void __launch_bounds__(kRowThreads, 8) route_rows_kernel(RowsArgs a, int P) {
+    extern __shared__ __align__(16) uint32_t rsm[];  // map + words + offsets, bitmap + offsets, or bitonic buffer [P]
     __shared__ int warp_tot[33];
     __shared__ int64_t red_lo[kRowThreads / 32], red_hi[kRowThreads / 32];
     const int64_t row = blockIdx.x;
@@ -126,37 +143,110 @@ __global__ void __launch_bounds__(kRowThreads) route_rows_kernel(RowsArgs a, int
         hi = max(hi, red_hi[w]);
     }
     int total = 0;
-    if (hi >= 0 && (hi - lo) / kRowWindowBits < kRowMaxWindows) {
-        for (int64_t w0 = lo; w0 <= hi; w0 += kRowWindowBits) {
-            const int64_t span = (hi - w0 + 1) < kRowWindowBits ? (hi - w0 + 1) : (int64_t)kRowWindowBits;
+    if (hi >= 0 && hi - lo < kRowMapKeys) {
+        uint8_t *flags = reinterpret_cast<uint8_t *>(rsm);
+        uint32_t *words = rsm + kRowMapKeys / 4;
+        int *woff = reinterpret_cast<int *>(words + kRowMapKeys / 32);
+        for (int64_t w0 = lo; w0 <= hi; w0 += kRowMapKeys) {  // one pass: the range fits the map
+            const int64_t span = (hi - w0 + 1) < kRowMapKeys ? (hi - w0 + 1) : (int64_t)kRowMapKeys;
             const int nwords = (int)((span + 31) / 32);
-            for (int i = tid; i < nwords; i += blockDim.x) rsm[i] = 0u;
+            for (int i = tid; i < nwords * 2; i += blockDim.x) reinterpret_cast<uint4 *>(flags)[i] = make_uint4(0, 0, 0, 0);
             __syncthreads();
             if (cached) {
 #pragma unroll
                 for (int j = 0; j < kRowCache; ++j) {
-                    const int64_t x = cache[j];  // -1 for invalid or missing slots
-                    if (x >= w0 && x < w0 + span) atomicOr(&rsm[(x - w0) >> 5], 1u << ((x - w0) & 31));
+                    const int64_t x = cache[j];
+                    if (x >= w0 && x < w0 + span) flags[x - w0] = 1;
                 }
             } else {
                 for (int64_t i = tid; i < a.K; i += blockDim.x) {
                     const int64_t x = load_route(a, b, q, i);
-                    if (x >= w0 && x < w0 + span) atomicOr(&rsm[(x - w0) >> 5], 1u << ((x - w0) & 31));
+                    if (x >= w0 && x < w0 + span) flags[x - w0] = 1;
                 }
             }
             __syncthreads();
             const int per = (nwords + blockDim.x - 1) / blockDim.x;
             const int s0 = min(nwords, tid * per), s1 = min(nwords, s0 + per);
             int local = 0;
-            for (int i = s0; i < s1; ++i) local += __popc(rsm[i]);
+            for (int i = s0; i < s1; ++i) {
+                const uint4 *f = reinterpret_cast<const uint4 *>(flags + i * 32);
+                const uint4 u = f[0], v = f[1];
+                const uint32_t bits = flag_nibble(u.x) | flag_nibble(u.y) << 4 | flag_nibble(u.z) << 8 |
+                                      flag_nibble(u.w) << 12 | flag_nibble(v.x) << 16 | flag_nibble(v.y) << 20 |
+                                      flag_nibble(v.z) << 24 | flag_nibble(v.w) << 28;
+                words[i] = bits;
+                local += __popc(bits);
+            }
             int win_total;
             int pos = total + block_exclusive_scan(local, warp_tot, win_total);
             for (int i = s0; i < s1; ++i) {
-                uint32_t bits = rsm[i];
-                while (bits) {
-                    const int bit = __ffs(bits) - 1;
-                    bits &= bits - 1;
-                    out[pos++] = (int32_t)(w0 + i * 32 + bit);
+                woff[i] = pos;
+                pos += __popc(words[i]);
+            }
+            __syncthreads();
+            for (int g = warp * 32; g < nwords; g += nwarps * 32) {
+                const int i = g + lane;
+                const uint32_t my_bits = i < nwords ? words[i] : 0u;
+                const int my_off = i < nwords ? woff[i] : 0;
+                uint32_t nz = __ballot_sync(0xffffffffu, my_bits != 0u);
+                while (nz) {
+                    const int src = __ffs(nz) - 1;
+                    nz &= nz - 1;
+                    const uint32_t bits = __shfl_sync(0xffffffffu, my_bits, src);
+                    const int off = __shfl_sync(0xffffffffu, my_off, src);
+                    if ((bits >> lane) & 1u)
+                        out[off + __popc(bits & ((1u << lane) - 1u))] = (int32_t)(w0 + (int64_t)(g + src) * 32 + lane);
+                }
+            }
+            total += win_total;
+            __syncthreads();
+        }
+    } else if (hi >= 0 && (hi - lo) / kRowWindowBits < kRowMaxWindows) {
+        uint32_t *words = rsm;
+        int *woff = reinterpret_cast<int *>(rsm + kRowWindowBits / 32);
+        for (int64_t w0 = lo; w0 <= hi; w0 += kRowWindowBits) {
+            const int64_t span = (hi - w0 + 1) < kRowWindowBits ? (hi - w0 + 1) : (int64_t)kRowWindowBits;
+            const int nwords = (int)((span + 31) / 32);
+            for (int i = tid; i < nwords; i += blockDim.x) words[i] = 0u;
+            __syncthreads();
+            if (cached) {
+#pragma unroll
+                for (int j = 0; j < kRowCache; ++j) {
+                    const int64_t x = cache[j];
+                    if (x >= w0 && x < w0 + span) atomicOr(&words[(x - w0) >> 5], 1u << ((x - w0) & 31));
+                }
+            } else {
+                for (int64_t i = tid; i < a.K; i += blockDim.x) {
+                    const int64_t x = load_route(a, b, q, i);
+                    if (x >= w0 && x < w0 + span) atomicOr(&words[(x - w0) >> 5], 1u << ((x - w0) & 31));
+                }
+            }
+            __syncthreads();
+            const int per = (nwords + blockDim.x - 1) / blockDim.x;
+            const int s0 = min(nwords, tid * per), s1 = min(nwords, s0 + per);
+            int local = 0;
+            for (int i = s0; i < s1; ++i) {
+                local += __popc(words[i]);
+            }
+            int win_total;
+            int pos = total + block_exclusive_scan(local, warp_tot, win_total);
+            for (int i = s0; i < s1; ++i) {
+                woff[i] = pos;
+                pos += __popc(words[i]);
+            }
+            __syncthreads();
+            for (int g = warp * 32; g < nwords; g += nwarps * 32) {
+                const int i = g + lane;
+                const uint32_t my_bits = i < nwords ? words[i] : 0u;
+                const int my_off = i < nwords ? woff[i] : 0;
+                uint32_t nz = __ballot_sync(0xffffffffu, my_bits != 0u);
+                while (nz) {
+                    const int src = __ffs(nz) - 1;
+                    nz &= nz - 1;
+                    const uint32_t bits = __shfl_sync(0xffffffffu, my_bits, src);
+                    const int off = __shfl_sync(0xffffffffu, my_off, src);
+                    if ((bits >> lane) & 1u)
+                        out[off + __popc(bits & ((1u << lane) - 1u))] = (int32_t)(w0 + (int64_t)(g + src) * 32 + lane);
                 }
             }
             total += win_total;
@@ -365,7 +455,7 @@ __global__ void __launch_bounds__(kOrderThreads) route_order_kernel(const int32_
 cudaError_t launch_route_rows(const RowsArgs &a, cudaStream_t s) {
     int P = 32;
     while (P < a.K) P <<= 1;
-    const size_t smem = std::max<size_t>((size_t)P * sizeof(int32_t), kRowWindowBits / 8);
+    const size_t smem = std::max<size_t>((size_t)P * sizeof(int32_t), kRowSmem);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(route_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
