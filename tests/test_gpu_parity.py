@@ -210,7 +210,7 @@ def test_autograd_matches_explicit_backward():
 
 def test_route_sets_wide_and_narrow_ranges():
     """Rows whose ids span a huge key range (sorted by the bitonic fallback) next
-    to narrow rows (sorted through the shared-memory bitmap): bit-exact."""
+    to narrow rows (sorted through the shared-memory byte map): bit-exact."""
     import torch
 
     import route_sparse_gqa_gb300 as qsa
@@ -221,6 +221,47 @@ def test_route_sets_wide_and_narrow_ranges():
     routes[0, ::3] = rng.integers(1000, 1200, size=(S_q // 3 + (S_q % 3 > 0), K))  # narrow rows
     routes[0, 1::5, :10] = 2**45 + 3
     routes[0, 7] = -1
+    dev = torch.device("cuda:0")
+    q = torch.zeros(1, S_q, 16, 256, dtype=torch.bfloat16, device=dev)
+    k = torch.zeros(1, S_kv, 2, 256, dtype=torch.bfloat16, device=dev)
+    plan = qsa.preprocess(q, k, k, torch.from_numpy(routes).to(dev))
+    ids, counts = plan.route_sets()
+    ids_ref, counts_ref = oracle.route_sets(routes, S_kv)
+    assert np.array_equal(counts.cpu().numpy(), counts_ref)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+
+
+def _rows_at_sort_boundaries(rng, K):
+    """Route rows whose valid ids span exactly the key ranges where route_rows changes
+    method: byte map up to 16384 keys, 65536-key bitmap windows up to 8 windows, bitonic
+    sort beyond; with contiguous 64-id runs, repeats, invalid values and empty rows."""
+    rows = []
+    for lo, span in ((5, 16383), (100, 16384), (0, 65535), (7, 65536), (3, 524287), (3, 524288), (11, 200_000)):
+        r = rng.integers(lo, lo + span + 1, size=K)
+        r[0], r[1] = lo, lo + span  # the range's ends
+        r[2:6] = r[6:10]  # repeats
+        r[10] = -1
+        r[11] = 2**40 + 5  # invalid, outside int32
+        rows.append(r)
+    for span in (8000, 200_000):  # runs of 64 consecutive ids, in generation order
+        starts = rng.choice(span // 64, size=(K + 63) // 64, replace=False) * 64 + 17
+        rows.append((starts[:, None] + np.arange(64)[None, :]).reshape(-1)[:K])
+    rows.append(np.full(K, -1))
+    rows.append(np.full(K, 2**40))
+    return np.stack(rows).astype(np.int64)
+
+
+@pytest.mark.parametrize("K", [96, 2600])  # route slots kept in registers / re-read for every window
+def test_route_sets_at_sort_method_boundaries(K):
+    """Every sort path of the route preprocessing and the range edges between them:
+    bit-exact against the oracle's route sets."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    rng = np.random.default_rng(77 + K)
+    routes = _rows_at_sort_boundaries(rng, K)[None]
+    S_q, S_kv = routes.shape[1], 600_000
     dev = torch.device("cuda:0")
     q = torch.zeros(1, S_q, 16, 256, dtype=torch.bfloat16, device=dev)
     k = torch.zeros(1, S_kv, 2, 256, dtype=torch.bfloat16, device=dev)
