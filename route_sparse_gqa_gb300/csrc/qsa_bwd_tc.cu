@@ -31,6 +31,7 @@
 // timeout is recorded in the status word, the roles wind down, in-flight
 // copies and MMAs are drained, and the TMEM is freed.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -522,19 +523,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 }  // namespace
 
 namespace {
+// The dynamic shared-memory limit is a property of the kernel on each device: it is set the
+// first time the kernels are launched on a device (devices 0-63 remembered in a bit mask).
 template <int D>
 cudaError_t set_bwd_smem() {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             BwdLayout<D>::kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(tc_bwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     BwdLayout<D>::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    return cudaSuccess;
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(tc_bwd_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdLayout<D>::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc_bwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 BwdLayout<D>::kSmemBytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 }  // namespace
 

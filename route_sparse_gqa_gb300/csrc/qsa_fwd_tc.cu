@@ -48,6 +48,7 @@
 // workspace status word, all roles wind down, in-flight copies and MMAs drain,
 // the TMEM is freed and the kernel returns.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -577,16 +578,19 @@ bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t) {
 }
 
 namespace {
+// The dynamic shared-memory limit is a property of the kernel on each device: it is set the
+// first time the kernel is launched on a device (devices 0-63 remembered in a bit mask).
 template <int D>
 cudaError_t set_fwd_smem() {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             FwdLayout<D>::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    return cudaSuccess;
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(tc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdLayout<D>::kSmemBytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 }  // namespace
 
