@@ -65,8 +65,9 @@ typedef enum qsa_status {
  *   LSE          : [B, Hq, S_q] float32, natural log
  * Hq must be a positive multiple of Hkv.  D is 256 as fa4_sparse_gqa_attention
  * fixes head_dim = 256 (the tensor-core tile kernels); D = 128 is also
- * accepted (tile kernels when Hq/Hkv divides 128 with at least two queries per
- * tile, else warp-level kernels) and D = 64 runs on the warp-level kernels.  S_kv may differ from S_q (context parallelism: local
+ * accepted (tile kernels when G = Hq/Hkv is a power of two from 4 to 64, as at
+ * D = 256; other G on warp-level kernels) and D = 64 runs on the warp-level
+ * kernels.  S_kv may differ from S_q (context parallelism: local
  * queries against gathered global K/V).  softmax_scale must be finite and > 0;
  * the pages' default 1/sqrt(D) is resolved by the caller.
  * Strides are in elements.  q/k/v need a unit last stride and, for the other
