@@ -16,8 +16,11 @@
  * Conventions shared by every entry point
  *   - Pointers named q, k, v, o, dout, dq, dk, dv, lse, routes and workspace
  *     are DEVICE pointers on the current CUDA device; *_host pointers are host.
- *   - The caller owns every buffer.  The library never allocates, frees or
- *     retains device memory and keeps no state between calls.
+ *   - The caller owns every buffer.  No entry point allocates or frees device
+ *     memory; the only device memory the library holds is the fixed array of
+ *     qsa_forward_no_alloc (below).  Between calls it keeps no state about
+ *     problems, only, per device, which kernels' shared-memory limits it has
+ *     already raised.
  *   - All device work is queued on `stream`; no entry point blocks the host
  *     except qsa_read_device_status, which says so.
  *   - BF16 tensors are passed as `const void*` holding IEEE bfloat16 values.
