@@ -61,6 +61,14 @@ qsa_status validate(const qsa_problem *p) {
     return QSA_OK;
 }
 
+// Key-major backward tuning (qsa_chunks.cu, qsa_bwd_km.cu).
+constexpr int64_t kKmMaxGroups = 16;            // groups of 128/G queries per work item at most
+constexpr int64_t kKmWindowBytes = 32ll << 20;  // fp32 dQ of one window of queries and one KV head
+constexpr int64_t kKmMaskWords = 4ll << 20;     // (64-row block, chunk) mask words at most (32 MiB)
+constexpr int64_t kKmMaxChunks = 16384;         // chunks per batch row (S_kv <= 2^20): counters in shared memory
+constexpr int64_t kKmMaxWindows = 1024;         // windows per launch of the queue builder
+constexpr int64_t kKmQueueBins = 8192;          // its counting-sort bins: windows x (groups + 1)
+
 Layout make_layout(const qsa_problem *p) {
     Layout L{};
     L.G = p->Hq / p->Hkv;
@@ -75,8 +83,9 @@ Layout make_layout(const qsa_problem *p) {
     size_t off = 0;
     L.off_status = off;
     off = align256(off + sizeof(DeviceStatus));
-    L.off_sched = off;  // work queue counters of the tile kernels: {next, done} for forward, then backward
-    off = align256(off + 4 * sizeof(int32_t));
+    // Work queue counters {next, done}: tile forward, tile backward, key-major backward.
+    L.off_sched = off;
+    off = align256(off + 6 * sizeof(int32_t));
     L.off_counts = off;
     off = align256(off + rows * sizeof(int32_t));
     L.off_ids = off;
@@ -89,6 +98,49 @@ Layout make_layout(const qsa_problem *p) {
     off = align256(off + tiles * L.max_chunks * L.T * sizeof(uint64_t));
     L.off_order = off;
     off = align256(off + tiles * sizeof(int32_t));
+    L.fwd_total = off;
+
+    // Key-major backward: reverse lists per aligned 64-key chunk, cut into work items.
+    L.NC = (p->S_kv + kChunkKeys - 1) / kChunkKeys;
+    if (L.T) {
+        const int64_t gd = L.G * p->D;
+        const int64_t w_max = std::max<int64_t>(256, kKmWindowBytes / (gd * (int64_t)sizeof(float)));
+        L.n_blk_b = (p->S_q + 63) / 64;
+        const int64_t wb_max = (w_max + 63) / 64;
+        L.n_win_b = (L.n_blk_b + wb_max - 1) / wb_max;
+        L.win_blocks = (L.n_blk_b + L.n_win_b - 1) / L.n_win_b;
+        L.max_groups = kKmMaxGroups;
+        L.cap_entries = rows * std::min<int64_t>(p->K, L.NC);
+        L.cap_items = L.cap_entries / (L.max_groups * L.T) + p->B * L.NC * L.n_win_b + 1;
+        const int64_t n_win = p->B * L.n_win_b;
+        L.km = L.NC <= kKmMaxChunks && p->B * L.n_blk_b * L.NC <= kKmMaskWords && L.cap_entries < INT32_MAX &&
+               L.cap_items * p->Hkv < INT32_MAX && n_win <= kKmMaxWindows &&
+               n_win * (L.max_groups + 1) <= kKmQueueBins && p->B * L.NC < INT32_MAX && rows * p->Hq < INT32_MAX;
+    }
+    if (L.km) {
+        const int64_t n_lists = p->B * L.NC;
+        const size_t words = (size_t)(p->B * L.n_blk_b * L.NC);
+        L.off_rmask = off;
+        off = align256(off + words * sizeof(uint64_t));
+        L.off_hoff = off;
+        off = align256(off + words * sizeof(int32_t));
+        L.off_list_start = off;
+        off = align256(off + (size_t)(n_lists + 1) * sizeof(int32_t));
+        L.off_eq = off;
+        off = align256(off + (size_t)L.cap_entries * sizeof(int32_t));
+        L.off_emask = off;
+        off = align256(off + (size_t)L.cap_entries * sizeof(uint64_t));
+        L.off_part_start = off;
+        off = align256(off + (size_t)(n_lists + 1) * sizeof(int32_t));
+        L.off_items = off;
+        off = align256(off + (size_t)L.cap_items * 4 * sizeof(int32_t));
+        L.off_sorted = off;
+        off = align256(off + (size_t)L.cap_items * sizeof(int32_t));
+        L.off_queue = off;
+        off = align256(off + (size_t)(L.cap_items * p->Hkv) * sizeof(int32_t));
+        L.off_kmeta = off;
+        off = align256(off + 4 * sizeof(int32_t));
+    }
     L.off_delta = off;
     off = align256(off + p->B * p->Hq * p->S_q * sizeof(float));
     // dK/dV accumulators: fp32, or (deterministic backward) an fp32 and a 32-bit integer word per element.
@@ -97,6 +149,9 @@ Layout make_layout(const qsa_problem *p) {
     off = align256(off + kv_acc);
     L.off_dv = off;
     off = align256(off + kv_acc);
+    // dQ accumulator of the key-major backward, same two forms.
+    L.off_dq = off;
+    if (L.km) off = align256(off + (size_t)rows * p->Hq * p->D * 8);
     L.total = off;
     return L;
 }
@@ -110,15 +165,19 @@ const T *at(const void *ws, size_t off) {
     return reinterpret_cast<const T *>(static_cast<const char *>(ws) + off);
 }
 
-qsa_status check_ws(const qsa_problem *p, const void *ws, size_t ws_bytes, Layout &L) {
+// full = true for the backward (every region), false for the preprocessing and the forward (the
+// prefix they use).
+qsa_status check_ws(const qsa_problem *p, const void *ws, size_t ws_bytes, Layout &L, bool full) {
     qsa_status st = validate(p);
     if (st != QSA_OK) return st;
     if (!ws) return fail(QSA_ERR_INVALID_ARGUMENT, "workspace is null");
     if (reinterpret_cast<uintptr_t>(ws) % 256 != 0)
         return fail(QSA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
     L = make_layout(p);
-    if (ws_bytes < L.total)
-        return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, L.total);
+    const size_t need = full ? L.total : L.fwd_total;
+    if (ws_bytes < need)
+        return fail(QSA_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, %s needs %zu", ws_bytes,
+                    full ? "the backward" : "the forward", need);
     return QSA_OK;
 }
 
@@ -180,6 +239,11 @@ TileArgs tile_args(const qsa_problem *p, const Layout &L, void *ws) {
 
 qsa_status report_error(qsa_status st, const char *msg) { return fail(st, "%s", msg); }
 
+size_t forward_workspace_bytes(const qsa_problem *p) {
+    if (validate(p) != QSA_OK) return 0;
+    return make_layout(p).fwd_total;
+}
+
 }  // namespace qsa
 
 namespace qsa {
@@ -188,7 +252,7 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
                          const void *o, const float *lse, const void *dout, void *dq, void *dk, void *dv,
                          float *dk_f32, float *dv_f32, bool deterministic, cudaStream_t stream) {
     Layout L;
-    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    qsa_status st = check_ws(p, ws, ws_bytes, L, true);
     if (st != QSA_OK) return st;
     if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
         return fail(QSA_ERR_INVALID_ARGUMENT, "null tensor pointer");
@@ -238,6 +302,8 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
     b.dk = static_cast<__nv_bfloat16 *>(dk);
     b.dv = static_cast<__nv_bfloat16 *>(dv);
     const size_t n_kv = (size_t)p->B * p->S_kv * p->Hkv * p->D;
+    const size_t n_q = (size_t)p->B * p->S_q * p->Hq * p->D;
+    const bool key_major = L.km && tc_backward_supported() && km_backward_shape_ok(b.f);
     cudaError_t e;
     if (deterministic) {
         // Fixed-point accumulators in the workspace; the caller's fp32 buffers (if any) receive the sums.
@@ -255,16 +321,65 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
         e = cudaMemsetAsync(b.dk_acc, 0, n_kv * sizeof(float), stream);
         if (e == cudaSuccess) e = cudaMemsetAsync(b.dv_acc, 0, n_kv * sizeof(float), stream);
     }
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the dK/dV accumulators");
+    if (e == cudaSuccess && key_major)
+        e = cudaMemsetAsync(at<char>(ws, L.off_dq), 0, n_q * (deterministic ? 8 : 4), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the gradient accumulators");
     e = launch_delta(b, stream);
     if (e != cudaSuccess) return cuda_fail(e, "delta launch");
-    const TileArgs ta = tile_args(p, L, ws);
-    if (L.T && tc_backward_supported() && tc_backward_shape_ok(b.f, ta)) {
-        e = launch_tc_backward(b, ta, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
+    if (key_major) {
+        ChunkArgs c{};
+        c.B = p->B;
+        c.S_q = p->S_q;
+        c.S_kv = p->S_kv;
+        c.K = p->K;
+        c.NC = L.NC;
+        c.Hkv = p->Hkv;
+        c.n_blk_b = L.n_blk_b;
+        c.win_blocks = L.win_blocks;
+        c.n_win_b = L.n_win_b;
+        c.slots = L.T;
+        c.max_groups = L.max_groups;
+        c.cap_entries = L.cap_entries;
+        c.cap_items = L.cap_items;
+        c.ids = at<int32_t>(ws, L.off_ids);
+        c.counts = at<int32_t>(ws, L.off_counts);
+        c.rmask = at<uint64_t>(ws, L.off_rmask);
+        c.hoff = at<int32_t>(ws, L.off_hoff);
+        c.list_start = at<int32_t>(ws, L.off_list_start);
+        c.e_q = at<int32_t>(ws, L.off_eq);
+        c.e_mask = at<uint64_t>(ws, L.off_emask);
+        c.part_start = at<int32_t>(ws, L.off_part_start);
+        c.items = at<int4>(ws, L.off_items);
+        c.sorted = at<int32_t>(ws, L.off_sorted);
+        c.queue = at<int32_t>(ws, L.off_queue);
+        c.meta = at<int32_t>(ws, L.off_kmeta);
+        e = launch_chunk_lists(c, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "reverse route list launch");
+        KmArgs k{};
+        k.NC = L.NC;
+        k.items = c.items;
+        k.queue = c.queue;
+        k.meta = c.meta;
+        k.e_q = c.e_q;
+        k.e_mask = c.e_mask;
+        k.sched = at<int32_t>(ws, L.off_sched) + 4;
+        if (deterministic) {
+            k.dq_fx.est = at<float>(ws, L.off_dq);
+            k.dq_fx.lo = at<uint32_t>(ws, L.off_dq + n_q * sizeof(float));
+        } else {
+            k.dq_acc = at<float>(ws, L.off_dq);
+        }
+        e = launch_km_backward(b, k, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "key-major backward launch");
     } else {
-        e = launch_rowwise_backward(b, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "rowwise backward launch");
+        const TileArgs ta = tile_args(p, L, ws);
+        if (L.T && tc_backward_supported() && tc_backward_shape_ok(b.f, ta)) {
+            e = launch_tc_backward(b, ta, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
+        } else {
+            e = launch_rowwise_backward(b, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "rowwise backward launch");
+        }
     }
     e = launch_convert_dkdv(b, stream);
     if (e != cudaSuccess) return cuda_fail(e, "dK/dV conversion launch");
@@ -286,7 +401,7 @@ size_t qsa_workspace_bytes(const qsa_problem *problem) {
 
 qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, size_t ws_bytes, cudaStream_t stream) {
     Layout L;
-    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    qsa_status st = check_ws(p, ws, ws_bytes, L, false);
     if (st != QSA_OK) return st;
     if (!routes) return fail(QSA_ERR_INVALID_ARGUMENT, "routes is null");
     if (reinterpret_cast<uintptr_t>(routes) % (p->route_bits / 8) != 0)
@@ -333,7 +448,7 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
 qsa_status qsa_forward(const qsa_problem *p, void *ws, size_t ws_bytes, const void *q, const void *k,
                        const void *v, void *o, float *lse, cudaStream_t stream) {
     Layout L;
-    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    qsa_status st = check_ws(p, ws, ws_bytes, L, false);
     if (st != QSA_OK) return st;
     if (!q || !k || !v || !o || !lse) return fail(QSA_ERR_INVALID_ARGUMENT, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
@@ -344,7 +459,7 @@ qsa_status qsa_forward(const qsa_problem *p, void *ws, size_t ws_bytes, const vo
     span_of(v, p->v_stride, p->B, p->S_kv, p->Hkv, p->D, v0, v1);
     const uintptr_t o0 = reinterpret_cast<uintptr_t>(o), o1 = o0 + 2 * (size_t)(p->B * p->S_q * p->Hq * p->D);
     const uintptr_t l0 = reinterpret_cast<uintptr_t>(lse), l1 = l0 + 4 * (size_t)(p->B * p->Hq * p->S_q);
-    const uintptr_t w0 = reinterpret_cast<uintptr_t>(ws), w1 = w0 + L.total;
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(ws), w1 = w0 + L.fwd_total;
     const uintptr_t in[4][2] = {{q0, q1}, {k0, k1}, {v0, v1}, {w0, w1}};
     for (auto &r : in)
         if (overlaps(o0, o1, r[0], r[1]) || overlaps(l0, l1, r[0], r[1]))
@@ -378,7 +493,7 @@ qsa_status qsa_backward_deterministic(const qsa_problem *p, void *ws, size_t ws_
 qsa_status qsa_copy_route_sets(const qsa_problem *p, const void *ws, size_t ws_bytes, int32_t *ids, int32_t *counts,
                                cudaStream_t stream) {
     Layout L;
-    qsa_status st = check_ws(p, ws, ws_bytes, L);
+    qsa_status st = check_ws(p, ws, ws_bytes, L, false);
     if (st != QSA_OK) return st;
     const size_t rows = (size_t)(p->B * p->S_q);
     cudaError_t e = cudaSuccess;

@@ -29,8 +29,16 @@ struct Layout {
     int64_t n_tiles;     // query tiles per batch row
     int64_t max_chunks;  // capacity of one tile's chunk list
     size_t off_status, off_sched, off_counts, off_ids, off_tile_nchunks, off_tile_keys, off_tile_masks, off_order;
-    size_t off_delta, off_dk, off_dv, total;  // off_dk/off_dv: 8 bytes per element (fp32 or fixed point)
+    size_t fwd_total;  // bytes the preprocessing and the forward use (everything before the backward's regions)
+    // Key-major backward (qsa_chunks.cu, qsa_bwd_km.cu); km = false when the problem does not take it.
+    bool km;
+    int64_t NC, n_blk_b, win_blocks, n_win_b, max_groups, cap_entries, cap_items;
+    size_t off_rmask, off_hoff, off_list_start, off_eq, off_emask, off_part_start, off_items, off_sorted, off_queue, off_kmeta;
+    size_t off_delta, off_dk, off_dv, off_dq, total;  // off_dk/off_dv/off_dq: 8 bytes per element (fp32 or fixed point)
 };
+
+// Workspace bytes the preprocessing and the forward need (a prefix of the full layout).
+size_t forward_workspace_bytes(const qsa_problem *p);
 
 // Device-side failure sites (DeviceStatus::where).
 enum Site : unsigned int {
@@ -41,6 +49,7 @@ enum Site : unsigned int {
     kSiteTileFwdKey = 11,
     kSiteTileBwdWait = 20,
     kSiteTileBwdKey = 21,
+    kSiteKeyBwdWait = 22,
     kSiteRouteScoreWait = 30,
 };
 
@@ -102,6 +111,37 @@ struct TilesArgs {
     int32_t *order;           // [B*n_tiles*Hkv] work items, heaviest first
 };
 cudaError_t launch_route_tiles(const TilesArgs &a, cudaStream_t s);
+
+// Key-major (reverse-route) lists, built from the sorted route sets for the
+// key-major backward (qsa_chunks.cu).  Key space is cut into aligned chunks of
+// 64 keys, NC per batch row; list (b, c) holds one entry per query row of
+// batch b that routes into chunk c: the query index and the 64-bit mask of the
+// chunk keys it routes to, in ascending query order.  Query rows are taken in
+// blocks of 64; a list is cut into parts (work items) of at most max_groups
+// groups of `slots` entries whose queries lie in one window of win_blocks
+// blocks; the work queue runs window by window, KV head by KV head within a
+// window, largest parts first.
+struct ChunkArgs {
+    int64_t B, S_q, S_kv, K, NC, Hkv;
+    int64_t n_blk_b;     // 64-row query blocks per batch row
+    int64_t win_blocks;  // blocks per window
+    int64_t n_win_b;     // windows per batch row
+    int64_t slots;       // queries per group (one MMA tile: 128 / G)
+    int64_t max_groups;  // groups per part at most
+    int64_t cap_entries, cap_items;
+    const int32_t *ids, *counts;
+    uint64_t *rmask;      // [B * n_blk_b, NC]: which of the block's 64 rows route into each chunk
+    int32_t *hoff;        // [B * n_blk_b, NC]: where the block's entries start inside each list
+    int32_t *list_start;  // [B * NC + 1]: exclusive scan of list lengths
+    int32_t *e_q;         // [cap_entries]: query index of each entry
+    uint64_t *e_mask;     // [cap_entries]: chunk keys the query routes to
+    int32_t *part_start;  // [B * NC + 1]: parts per list, then their exclusive scan
+    int4 *items;          // [cap_items]: {list, first entry, entries, window}
+    int32_t *sorted;      // [cap_items]: items by window, largest first
+    int32_t *queue;       // [cap_items * Hkv]: item * Hkv + KV head, in work order
+    int32_t *meta;        // {entries, items, queue length, overflow flag}
+};
+cudaError_t launch_chunk_lists(const ChunkArgs &a, cudaStream_t s);
 
 struct AttnArgs {
     int64_t B, S_q, S_kv, Hq, Hkv, K, G;

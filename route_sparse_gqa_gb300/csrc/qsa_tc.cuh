@@ -62,6 +62,20 @@ bool tc_forward_supported();
 bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t);
 cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s);
 
+// Key-major backward (qsa_bwd_km.cu): reverse lists from qsa_chunks.cu and the
+// fp32 dQ accumulator it scatter-adds into.
+struct KmArgs {
+    int64_t NC;  // aligned 64-key chunks per batch row
+    const int4 *items;
+    const int32_t *queue, *meta, *e_q;
+    const uint64_t *e_mask;
+    int32_t *sched;  // work queue counters {next, done}
+    float *dq_acc;   // fp32 [B, S_q, Hq, D] (zeroed), or null in deterministic mode
+    FxAcc dq_fx;     // deterministic mode: exact accumulators
+};
+bool km_backward_shape_ok(const AttnArgs &a);
+cudaError_t launch_km_backward(const BwdArgs &b, const KmArgs &k, cudaStream_t s);
+
 bool tc_backward_supported();
 bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t);
 cudaError_t launch_tc_backward(const BwdArgs &b, const TileArgs &t, cudaStream_t s);
