@@ -515,32 +515,26 @@ __global__ void __launch_bounds__(kThreads, 1) km_bwd_kernel(const __grid_consta
                     }
                     tc_fence_after();
                     float *acc = (kDet ? p.dq_fx.est : p.dq_acc) + h * 128 + dl;
-                    // 64 rows at a time; the TMEM is released once the second half has been read.  Rows come in
-                    // blocks of eight heads of one query (G >= 8): one accumulator row address per block, then
-                    // eight reductions at fixed offsets.
+                    // All 128 columns to registers, the TMEM released, then the reductions.  Rows come in blocks
+                    // of eight heads of one query (G >= 8): one accumulator row address per block, then eight
+                    // reductions at fixed offsets.
+                    uint32_t v[4][32];
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        uint32_t v[2][32];
-                        tmem_ld32(trow + L::kTmemDQT + part * 64, v[0]);
-                        tmem_ld32(trow + L::kTmemDQT + part * 64 + 32, v[1]);
-                        tmem_ld_wait();
-                        if (part == 1) {
-                            tc_fence_before();
-                            mbar_arrive(bars + kDQFree);
-                        }
+                    for (int b4 = 0; b4 < 4; ++b4) tmem_ld32(trow + L::kTmemDQT + b4 * 32, v[b4]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(bars + kDQFree);
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const int r0 = part * 64 + jj * 8;  // first row of the block
-                            const int slot = r0 >> gshift;
-                            const int64_t q = __shfl_sync(0xffffffffu, my_q, slot);
-                            if (r0 < nrows) {
-                                const int64_t off = ((it.b * p.S_q + q) * p.Hq + it.g * p.G + (r0 & gmask)) * D;
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int r0 = jj * 8;  // first row of the block
+                        const int64_t q = __shfl_sync(0xffffffffu, my_q, r0 >> gshift);
+                        if (r0 < nrows) {
+                            const int64_t off = ((it.b * p.S_q + q) * p.Hq + it.g * p.G + (r0 & gmask)) * D;
 #pragma unroll
-                                for (int t = 0; t < 8; ++t) {
-                                    const float x = __uint_as_float(v[(jj * 8 + t) >> 5][(jj * 8 + t) & 31]);
-                                    if (kDet) red_add_fx(acc + off + t * D, p.dq_fx.lo + (acc - p.dq_fx.est) + off + t * D, x);
-                                    else red_add_f32(acc + off + t * D, x);
-                                }
+                            for (int t = 0; t < 8; ++t) {
+                                const float x = __uint_as_float(v[jj >> 2][(jj & 3) * 8 + t]);
+                                if (kDet) red_add_fx(acc + off + t * D, p.dq_fx.lo + (acc - p.dq_fx.est) + off + t * D, x);
+                                else red_add_f32(acc + off + t * D, x);
                             }
                         }
                     }

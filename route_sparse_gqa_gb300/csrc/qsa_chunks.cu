@@ -64,7 +64,7 @@ __device__ __forceinline__ int block_scan_excl(int x, int *warp_tot, int &total)
 }
 
 constexpr int kBlockRows = 64;     // query rows per block (one 64-bit row mask)
-constexpr int kBlockThreads = 512;
+constexpr int kBlockThreads = 1024;  // 32 warps: two rows of the block each
 
 // Walks the sorted ids of row r (of the block) 32 at a time and calls
 // emit(c, m) once per chunk c the row routes into, with m the mask of the
@@ -75,33 +75,45 @@ template <bool kMask, typename F>
 __device__ __forceinline__ void walk_row_chunks(const int32_t *ids, int n, int lane, F &&emit) {
     int carry_c = -1;
     uint64_t carry_m = 0;
-    for (int base = 0; base < n; base += 32) {
-        const int i = base + lane;
-        const bool valid = i < n;
-        const int32_t id = valid ? __ldg(ids + i) : 0;
-        const int c = valid ? (id >> 6) : -1;
-        uint64_t m = 0;
-        if (kMask) {
-            m = valid ? (1ull << (id & 63)) : 0ull;
-            // Segmented inclusive OR: the lanes of one chunk are contiguous (ids ascend).
+    constexpr int kAhead = 4;  // 32-id batches loaded together (independent loads in flight)
+    for (int base0 = 0; base0 < n; base0 += 32 * kAhead) {
+        int32_t idv[kAhead];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint64_t y = __shfl_up_sync(0xffffffffu, m, o);
-                const int cy = __shfl_up_sync(0xffffffffu, c, o);
-                if (lane >= o && cy == c) m |= y;
-            }
-            if (valid && c == carry_c) m |= carry_m;  // the carried run continues here
+        for (int u = 0; u < kAhead; ++u) {
+            const int i = base0 + 32 * u + lane;
+            idv[u] = i < n ? __ldg(ids + i) : 0;
         }
-        const int c0 = __shfl_sync(0xffffffffu, c, 0);
-        // The carried run ended with the previous 32 ids: emit it (its chunk differs from all below).
-        if (carry_c >= 0 && c0 != carry_c && lane == 0) emit(carry_c, carry_m);
-        const int c_next = __shfl_down_sync(0xffffffffu, c, 1);
-        const int n_here = n - base < 32 ? n - base : 32;
-        const bool last_lane = lane == n_here - 1;
-        const bool more = base + 32 < n;
-        if (valid && (last_lane || c_next != c) && !(last_lane && more)) emit(c, m);
-        carry_c = more ? __shfl_sync(0xffffffffu, c, 31) : -1;
-        carry_m = more ? __shfl_sync(0xffffffffu, m, 31) : 0ull;
+#pragma unroll
+        for (int u = 0; u < kAhead; ++u) {
+            const int base = base0 + 32 * u;
+            if (base >= n) break;
+            const int i = base + lane;
+            const bool valid = i < n;
+            const int32_t id = idv[u];
+            const int c = valid ? (id >> 6) : -1;
+            uint64_t m = 0;
+            if (kMask) {
+                m = valid ? (1ull << (id & 63)) : 0ull;
+                // Segmented inclusive OR: the lanes of one chunk are contiguous (ids ascend).
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint64_t y = __shfl_up_sync(0xffffffffu, m, o);
+                    const int cy = __shfl_up_sync(0xffffffffu, c, o);
+                    if (lane >= o && cy == c) m |= y;
+                }
+                if (valid && c == carry_c) m |= carry_m;  // the carried run continues here
+            }
+            const int c0 = __shfl_sync(0xffffffffu, c, 0);
+            // The carried run ended with the previous 32 ids: emit it (its chunk differs from all below).
+            if (carry_c >= 0 && c0 != carry_c && lane == 0) emit(carry_c, carry_m);
+            const int c_next = __shfl_down_sync(0xffffffffu, c, 1);
+            const int n_here = n - base < 32 ? n - base : 32;
+            const bool last_lane = lane == n_here - 1;
+            const bool more = base + 32 < n;
+            if (valid && (last_lane || c_next != c) && !(last_lane && more)) emit(c, m);
+            carry_c = more ? __shfl_sync(0xffffffffu, c, 31) : -1;
+            carry_m = more ? __shfl_sync(0xffffffffu, m, 31) : 0ull;
+        }
     }
 }
 
@@ -124,29 +136,42 @@ __global__ void __launch_bounds__(kBlockThreads) chunk_mask_kernel(ChunkArgs a) 
     for (int64_t c = threadIdx.x; c < a.NC; c += blockDim.x) out[c] = tbl[c];
 }
 
-// One thread per list (b, c): block offsets inside the list, the list length
-// (to list_start[l]) and the number of parts (to part_start[l]); both are
-// scanned next.
-__global__ void chunk_colscan_kernel(ChunkArgs a) {
-    const int64_t l = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (l >= a.B * a.NC) return;
+// One warp per list (b, c): block offsets inside the list (a warp scan over 32
+// blocks at a time), the list length (to list_start[l]) and the number of
+// parts, window by window (to part_start[l]); both are scanned next.
+__global__ void __launch_bounds__(256) chunk_colscan_kernel(ChunkArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t l = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (l >= a.B * a.NC) return;  // whole warps
     const int64_t b = l / a.NC, c = l % a.NC;
-    const int64_t per = a.max_groups * a.slots;
-    int32_t run = 0, win0 = 0, parts = 0;
     const uint64_t *rm = a.rmask + b * a.n_blk_b * a.NC + c;
     int32_t *ho = a.hoff + b * a.n_blk_b * a.NC + c;
-#pragma unroll 4
-    for (int64_t k = 0; k < a.n_blk_b; ++k) {
-        if (k % a.win_blocks == 0) {
-            parts += (int32_t)((run - win0 + per - 1) / per);
-            win0 = run;
+    int32_t run = 0;
+    for (int64_t k0 = 0; k0 < a.n_blk_b; k0 += 32) {
+        const int64_t k = k0 + lane;
+        const int v = k < a.n_blk_b ? __popcll(rm[k * a.NC]) : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
-        ho[k * a.NC] = run;
-        run += __popcll(rm[k * a.NC]);
+        if (k < a.n_blk_b) ho[k * a.NC] = run + incl - v;
+        run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    parts += (int32_t)((run - win0 + per - 1) / per);
-    a.list_start[l] = run;
-    a.part_start[l] = parts;
+    __syncwarp();
+    if (lane == 0) {
+        const int64_t per = a.max_groups * a.slots;
+        int32_t parts = 0;
+        for (int64_t w = 0; w < a.n_win_b; ++w) {
+            const int64_t k0 = w * a.win_blocks, k1 = k0 + a.win_blocks;
+            const int32_t s0 = ho[k0 * a.NC];
+            const int32_t s1 = k1 < a.n_blk_b ? ho[k1 * a.NC] : run;
+            parts += (int32_t)((s1 - s0 + per - 1) / per);
+        }
+        a.list_start[l] = run;
+        a.part_start[l] = parts;
+    }
 }
 
 // One CTA per block again: every (row, chunk) entry with its key mask, at the
@@ -298,7 +323,7 @@ cudaError_t launch_chunk_lists(const ChunkArgs &a, cudaStream_t s) {
     }
     const unsigned list_blocks = (unsigned)((n_lists + 255) / 256);
     chunk_mask_kernel<<<(unsigned)n_blk, kBlockThreads, smem_mask, s>>>(a);
-    chunk_colscan_kernel<<<list_blocks, 256, 0, s>>>(a);
+    chunk_colscan_kernel<<<(unsigned)((n_lists * 32 + 255) / 256), 256, 0, s>>>(a);
     scan_kernel<<<1, kScanThreads, 0, s>>>(a.list_start, n_lists, a.meta + 0);
     scan_kernel<<<1, kScanThreads, 0, s>>>(a.part_start, n_lists, a.meta + 1);
     chunk_fill_kernel<<<(unsigned)n_blk, kBlockThreads, smem_fill, s>>>(a);
