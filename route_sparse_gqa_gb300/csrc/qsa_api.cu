@@ -83,9 +83,10 @@ Layout make_layout(const qsa_problem *p) {
     size_t off = 0;
     L.off_status = off;
     off = align256(off + sizeof(DeviceStatus));
-    // Work queue counters {next, done}: tile forward, tile backward, key-major backward.
+    // Work queue counters {next, done}: tile forward, tile backward, key-major backward, key-major forward
+    // row-max pass, key-major forward output pass.
     L.off_sched = off;
-    off = align256(off + 6 * sizeof(int32_t));
+    off = align256(off + 10 * sizeof(int32_t));
     L.off_counts = off;
     off = align256(off + rows * sizeof(int32_t));
     L.off_ids = off;
@@ -98,7 +99,6 @@ Layout make_layout(const qsa_problem *p) {
     off = align256(off + tiles * L.max_chunks * L.T * sizeof(uint64_t));
     L.off_order = off;
     off = align256(off + tiles * sizeof(int32_t));
-    L.fwd_total = off;
 
     // Key-major backward: reverse lists per aligned 64-key chunk, cut into work items.
     L.NC = (p->S_kv + kChunkKeys - 1) / kChunkKeys;
@@ -138,9 +138,18 @@ Layout make_layout(const qsa_problem *p) {
         off = align256(off + (size_t)L.cap_items * sizeof(int32_t));
         L.off_queue = off;
         off = align256(off + (size_t)(L.cap_items * p->Hkv) * sizeof(int32_t));
-        L.off_kmeta = off;
-        off = align256(off + 4 * sizeof(int32_t));
+        L.off_kmeta = off;  // {entries, items, queue length, overflow, forward path choice, -, tile chunks, groups}
+        off = align256(off + 8 * sizeof(int32_t));
+        // Key-major forward: row maxima and sums, and the fp32 accumulator it shares with the backward's dQ
+        // (8 bytes per element for the deterministic backward's exact sums).
+        L.off_mrow = off;
+        off = align256(off + (size_t)(p->B * p->Hq * p->S_q) * sizeof(int32_t));
+        L.off_lrow = off;
+        off = align256(off + (size_t)(p->B * p->Hq * p->S_q) * sizeof(float));
+        L.off_dq = off;
+        off = align256(off + (size_t)rows * p->Hq * p->D * 8);
     }
+    L.fwd_total = off;
     L.off_delta = off;
     off = align256(off + p->B * p->Hq * p->S_q * sizeof(float));
     // dK/dV accumulators: fp32, or (deterministic backward) an fp32 and a 32-bit integer word per element.
@@ -149,9 +158,6 @@ Layout make_layout(const qsa_problem *p) {
     off = align256(off + kv_acc);
     L.off_dv = off;
     off = align256(off + kv_acc);
-    // dQ accumulator of the key-major backward, same two forms.
-    L.off_dq = off;
-    if (L.km) off = align256(off + (size_t)rows * p->Hq * p->D * 8);
     L.total = off;
     return L;
 }
@@ -235,6 +241,37 @@ TileArgs tile_args(const qsa_problem *p, const Layout &L, void *ws) {
     return t;
 }
 
+// The reverse lists' arguments (qsa_chunks.cu) for this problem's workspace.
+ChunkArgs chunk_args(const qsa_problem *p, const Layout &L, void *ws) {
+    ChunkArgs c{};
+    c.B = p->B;
+    c.S_q = p->S_q;
+    c.S_kv = p->S_kv;
+    c.K = p->K;
+    c.NC = L.NC;
+    c.Hkv = p->Hkv;
+    c.n_blk_b = L.n_blk_b;
+    c.win_blocks = L.win_blocks;
+    c.n_win_b = L.n_win_b;
+    c.slots = L.T;
+    c.max_groups = L.max_groups;
+    c.cap_entries = L.cap_entries;
+    c.cap_items = L.cap_items;
+    c.ids = at<int32_t>(ws, L.off_ids);
+    c.counts = at<int32_t>(ws, L.off_counts);
+    c.rmask = at<uint64_t>(ws, L.off_rmask);
+    c.hoff = at<int32_t>(ws, L.off_hoff);
+    c.list_start = at<int32_t>(ws, L.off_list_start);
+    c.e_q = at<int32_t>(ws, L.off_eq);
+    c.e_mask = at<uint64_t>(ws, L.off_emask);
+    c.part_start = at<int32_t>(ws, L.off_part_start);
+    c.items = at<int4>(ws, L.off_items);
+    c.sorted = at<int32_t>(ws, L.off_sorted);
+    c.queue = at<int32_t>(ws, L.off_queue);
+    c.meta = at<int32_t>(ws, L.off_kmeta);
+    return c;
+}
+
 }  // namespace
 
 qsa_status report_error(qsa_status st, const char *msg) { return fail(st, "%s", msg); }
@@ -303,7 +340,8 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
     b.dv = static_cast<__nv_bfloat16 *>(dv);
     const size_t n_kv = (size_t)p->B * p->S_kv * p->Hkv * p->D;
     const size_t n_q = (size_t)p->B * p->S_q * p->Hq * p->D;
-    const bool key_major = L.km && tc_backward_supported() && km_backward_shape_ok(b.f);
+    const bool key_major = L.km && tc_backward_supported() && km_backward_shape_ok(b.f) &&
+                           forced_path("QSA_DEBUG_BACKWARD_PATH") != 0;
     cudaError_t e;
     if (deterministic) {
         // Fixed-point accumulators in the workspace; the caller's fp32 buffers (if any) receive the sums.
@@ -327,34 +365,7 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
     e = launch_delta(b, stream);
     if (e != cudaSuccess) return cuda_fail(e, "delta launch");
     if (key_major) {
-        ChunkArgs c{};
-        c.B = p->B;
-        c.S_q = p->S_q;
-        c.S_kv = p->S_kv;
-        c.K = p->K;
-        c.NC = L.NC;
-        c.Hkv = p->Hkv;
-        c.n_blk_b = L.n_blk_b;
-        c.win_blocks = L.win_blocks;
-        c.n_win_b = L.n_win_b;
-        c.slots = L.T;
-        c.max_groups = L.max_groups;
-        c.cap_entries = L.cap_entries;
-        c.cap_items = L.cap_items;
-        c.ids = at<int32_t>(ws, L.off_ids);
-        c.counts = at<int32_t>(ws, L.off_counts);
-        c.rmask = at<uint64_t>(ws, L.off_rmask);
-        c.hoff = at<int32_t>(ws, L.off_hoff);
-        c.list_start = at<int32_t>(ws, L.off_list_start);
-        c.e_q = at<int32_t>(ws, L.off_eq);
-        c.e_mask = at<uint64_t>(ws, L.off_emask);
-        c.part_start = at<int32_t>(ws, L.off_part_start);
-        c.items = at<int4>(ws, L.off_items);
-        c.sorted = at<int32_t>(ws, L.off_sorted);
-        c.queue = at<int32_t>(ws, L.off_queue);
-        c.meta = at<int32_t>(ws, L.off_kmeta);
-        e = launch_chunk_lists(c, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "reverse route list launch");
+        const ChunkArgs c = chunk_args(p, L, ws);
         KmArgs k{};
         k.NC = L.NC;
         k.items = c.items;
@@ -442,6 +453,15 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
         e = launch_route_tiles(t, stream);
         if (e != cudaSuccess) return cuda_fail(e, "route_tiles launch");
     }
+    if (L.km) {
+        // Reverse lists for the key-major kernels, and the forward path choice.
+        const ChunkArgs c = chunk_args(p, L, ws);
+        e = launch_chunk_lists(c, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "reverse route list launch");
+        e = launch_km_choose(at<int32_t>(ws, L.off_tile_nchunks), p->B * L.n_tiles, c.list_start, p->B * L.NC, L.T,
+                             c.meta + 4, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "path choice launch");
+    }
     return QSA_OK;
 }
 
@@ -469,8 +489,28 @@ qsa_status qsa_forward(const qsa_problem *p, void *ws, size_t ws_bytes, const vo
     cudaError_t e;
     const TileArgs ta = tile_args(p, L, ws);
     if (L.T && tc_forward_supported() && tc_forward_shape_ok(a, ta)) {
-        e = launch_tc_forward(a, ta, static_cast<__nv_bfloat16 *>(o), lse, stream);
+        // With reverse lists, the tile and key-major forwards are both launched; the device-side choice
+        // made at preprocessing lets one of them run and the other return at once.
+        const bool km = L.km && km_forward_shape_ok(a);
+        const int32_t *choice = km ? at<int32_t>(ws, L.off_kmeta) + 4 : nullptr;
+        e = launch_tc_forward(a, ta, static_cast<__nv_bfloat16 *>(o), lse, choice, stream);
         if (e != cudaSuccess) return cuda_fail(e, "tile forward launch");
+        if (km) {
+            KfArgs k{};
+            k.NC = L.NC;
+            k.items = at<int4>(ws, L.off_items);
+            k.queue = at<int32_t>(ws, L.off_queue);
+            k.meta = at<int32_t>(ws, L.off_kmeta);
+            k.e_q = at<int32_t>(ws, L.off_eq);
+            k.e_mask = at<uint64_t>(ws, L.off_emask);
+            k.sched = at<int32_t>(ws, L.off_sched) + 6;
+            k.mrow = at<int32_t>(ws, L.off_mrow);
+            k.lrow = at<float>(ws, L.off_lrow);
+            k.o_acc = at<float>(ws, L.off_dq);
+            k.choice = choice;
+            e = launch_km_forward(a, k, static_cast<__nv_bfloat16 *>(o), lse, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "key-major forward launch");
+        }
     } else {
         e = launch_rowwise_forward(a, static_cast<__nv_bfloat16 *>(o), lse, stream);
         if (e != cudaSuccess) return cuda_fail(e, "rowwise forward launch");

@@ -105,6 +105,7 @@ struct FwdParams {
     int32_t *sched;  // work queue counters {next, done}
     __nv_bfloat16 *o;
     float *lse;
+    const int32_t *choice;  // null, or 1 when the key-major forward runs instead
     DeviceStatus *status;
 };
 
@@ -186,6 +187,7 @@ __device__ __forceinline__ void load_q_row(const FwdParams &p, const Item &it, i
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
+    if (p.choice && *p.choice == 1) return;  // uniform over the grid
     using L = FwdLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -594,7 +596,8 @@ cudaError_t set_fwd_smem() {
 }
 }  // namespace
 
-cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s) {
+cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse,
+                              const int32_t *choice, cudaStream_t s) {
     FwdParams p;
     memset(&p, 0, sizeof(p));
     if (!tc_encode_tile_map(&p.q_map, a.q, a.Hq, a.S_q, a.B, a.qs2, a.qs1, a.qs0, a.G, t.T, a.D))
@@ -625,6 +628,7 @@ cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat1
     p.sched = t.sched;  // forward counters
     p.o = o;
     p.lse = lse;
+    p.choice = choice;
     p.status = a.status;
     for (int64_t g0 = 0; g0 < a.Hkv; g0 += g_per_launch) {
         const int64_t n_g = std::min<int64_t>(g_per_launch, a.Hkv - g0);

@@ -30,10 +30,11 @@ struct Layout {
     int64_t max_chunks;  // capacity of one tile's chunk list
     size_t off_status, off_sched, off_counts, off_ids, off_tile_nchunks, off_tile_keys, off_tile_masks, off_order;
     size_t fwd_total;  // bytes the preprocessing and the forward use (everything before the backward's regions)
-    // Key-major backward (qsa_chunks.cu, qsa_bwd_km.cu); km = false when the problem does not take it.
+    // Key-major paths (qsa_chunks.cu, qsa_fwd_km.cu, qsa_bwd_km.cu); km = false when the problem does not take them.
     bool km;
     int64_t NC, n_blk_b, win_blocks, n_win_b, max_groups, cap_entries, cap_items;
     size_t off_rmask, off_hoff, off_list_start, off_eq, off_emask, off_part_start, off_items, off_sorted, off_queue, off_kmeta;
+    size_t off_mrow, off_lrow;  // key-major forward row statistics
     size_t off_delta, off_dk, off_dv, off_dq, total;  // off_dk/off_dv/off_dq: 8 bytes per element (fp32 or fixed point)
 };
 
@@ -50,6 +51,7 @@ enum Site : unsigned int {
     kSiteTileBwdWait = 20,
     kSiteTileBwdKey = 21,
     kSiteKeyBwdWait = 22,
+    kSiteKeyFwdWait = 23,
     kSiteRouteScoreWait = 30,
 };
 

@@ -60,7 +60,10 @@ bool tc_head_major_order(const AttnArgs &a, int64_t n_g);
 
 bool tc_forward_supported();
 bool tc_forward_shape_ok(const AttnArgs &a, const TileArgs &t);
-cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse, cudaStream_t s);
+// choice: null, or a device flag; the tile forward returns at once when *choice == 1 (the key-major
+// forward runs instead).
+cudaError_t launch_tc_forward(const AttnArgs &a, const TileArgs &t, __nv_bfloat16 *o, float *lse,
+                              const int32_t *choice, cudaStream_t s);
 
 // Key-major backward (qsa_bwd_km.cu): reverse lists from qsa_chunks.cu and the
 // fp32 dQ accumulator it scatter-adds into.
@@ -75,6 +78,26 @@ struct KmArgs {
 };
 bool km_backward_shape_ok(const AttnArgs &a);
 cudaError_t launch_km_backward(const BwdArgs &b, const KmArgs &k, cudaStream_t s);
+
+// Key-major forward (qsa_fwd_km.cu): the same reverse lists and work queue, two passes (row maxima, then
+// outputs reduced into fp32 accumulators) and a final division.  launch_km_choose decides on the device,
+// from the preprocessed routes, whether it or the tile forward runs: choice[0] = 1 for the key-major one.
+struct KfArgs {
+    int64_t NC;
+    const int4 *items;
+    const int32_t *queue, *meta, *e_q;
+    const uint64_t *e_mask;
+    int32_t *sched;   // two pairs of work queue counters {next, done}: row-max pass, output pass
+    int32_t *mrow;    // [B, Hq, S_q]
+    float *lrow;      // [B, Hq, S_q]
+    float *o_acc;     // [B, S_q, Hq, D] fp32
+    const int32_t *choice;
+};
+bool km_forward_shape_ok(const AttnArgs &a);
+int forced_path(const char *env_var);  // debug override of a path choice: 0 tile, 1 key-major, -1 none
+cudaError_t launch_km_choose(const int32_t *tile_nchunks, int64_t n_tiles, const int32_t *list_start,
+                             int64_t n_lists, int64_t slots, int32_t *choice, cudaStream_t s);
+cudaError_t launch_km_forward(const AttnArgs &a, const KfArgs &k, __nv_bfloat16 *o, float *lse, cudaStream_t s);
 
 bool tc_backward_supported();
 bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t);
