@@ -93,11 +93,16 @@ QSA_API qsa_status qsa_check_problem(const qsa_problem *problem);
 /* Bytes of device workspace qsa_preprocess/qsa_forward/qsa_backward need for
  * this problem (256-byte aligned base required), or 0 if the problem is
  * invalid.  The workspace holds the preprocessed routes (per-row sorted unique
- * IDs and counts, per-tile key lists and membership masks, the work order),
- * the backward pass's fp32 row statistics and dK/dV accumulators, the work
- * queue counters of the attention kernels, and a device status word.  Every
- * call that takes the workspace updates it, so calls sharing one workspace
- * must be ordered (one stream, or events between streams). */
+ * IDs and counts; per-query-tile key lists and membership masks; per 64-key
+ * chunk, the lists of query rows that route into it, cut into work items),
+ * the forward's row statistics and the fp32 accumulator shared by the
+ * key-major forward's O and the backward's dQ, the backward's fp32 row
+ * statistics and dK/dV accumulators, the work queue counters of the attention
+ * kernels, and a device status word.  qsa_preprocess and qsa_forward use only
+ * a leading part of the layout and accept a workspace of that size; the
+ * backward needs all of it.  Every call that takes the workspace updates it,
+ * so calls sharing one workspace must be ordered (one stream, or events
+ * between streams). */
 QSA_API size_t qsa_workspace_bytes(const qsa_problem *problem);
 
 /* Route preprocessing (fa4_qsa _preprocess and _block_kinds/_compact_blocks
@@ -121,8 +126,10 @@ QSA_API qsa_status qsa_forward(const qsa_problem *problem, void *workspace, size
 
 /* First-order backward (fa4_sparse_gqa_attention: first-order autograd only,
  * nondeterministic accumulation accepted).  Given O and LSE from qsa_forward and
- * dout = dL/dO, writes dq [B,S_q,Hq,D], dk and dv [B,S_kv,Hkv,D] in BF16.  dK/dV
- * are accumulated by fp32 scatter-add; when dk_f32/dv_f32 are non-null they
+ * dout = dL/dO, writes dq [B,S_q,Hq,D], dk and dv [B,S_kv,Hkv,D] in BF16.  The
+ * sums run in fp32, partly by scatter-add in an order that varies between calls
+ * (dQ too on the key-major path), so repeated calls agree within rounding, not
+ * bit for bit (qsa_backward_deterministic does); when dk_f32/dv_f32 are non-null they
  * receive those fp32 sums (same shape, float32) and serve as the accumulators,
  * otherwise the workspace does.  Rows with no valid route give dq = 0 and add
  * nothing to dk/dv.  Outputs must not overlap the inputs or each other. */
@@ -139,8 +146,9 @@ QSA_API qsa_status qsa_backward(const qsa_problem *problem, void *workspace, siz
  * is nearest to the fp32 estimate (which stays far closer than the 2^7 that
  * requires).  The results depend on the inputs only; they are converted to fp32
  * (dk_f32/dv_f32 when non-null) and BF16.  Resolution 2^-24 per contribution.
- * dQ is accumulated in a fixed order in either call.  Costs one more 32-bit
- * reduction per contribution than qsa_backward.  Arguments, layouts and errors
+ * dQ is summed the same way where it is scattered (key-major path) and in a
+ * fixed order otherwise.  Costs one more 32-bit reduction per contribution
+ * than qsa_backward.  Arguments, layouts and errors
  * are those of qsa_backward; the accumulators live in the workspace. */
 QSA_API qsa_status qsa_backward_deterministic(const qsa_problem *problem, void *workspace, size_t ws_bytes,
                                               const void *q, const void *k, const void *v, const void *o,
@@ -161,15 +169,23 @@ QSA_API qsa_status qsa_copy_route_sets(const qsa_problem *problem, const void *w
  * plugin's enqueue, or a latency-critical loop that cannot afford an
  * allocation's implicit synchronisation).  Instead of a caller workspace it
  * uses one fixed 32 MiB device array inside the library, which every GPU that
- * loads it keeps until the process exits; problems whose
- * qsa_workspace_bytes() exceeds 32 MiB are rejected with QSA_ERR_UNSUPPORTED.
- * The first call on a device looks up that array's device address (with the
- * device current), so make that first call before any stream capture.  All
- * calls share the one array and it keeps the last call's contents: calls that
- * overlap on the GPU (other streams, other host threads) race with each other.
- * Outputs and conventions are those of qsa_preprocess + qsa_forward. */
+ * loads it keeps until the process exits; problems whose preprocessing and
+ * forward regions of the workspace exceed 32 MiB are rejected with
+ * QSA_ERR_UNSUPPORTED.  The first call on a device looks up that array's
+ * device address (with the device current) and keeps it, so make that first
+ * call before any stream capture, and make no further call after
+ * cudaDeviceReset on that device.  All calls share the one array and it keeps
+ * the last call's contents: calls that overlap on the GPU (other streams,
+ * other host threads) race with each other.  Outputs and conventions are
+ * those of qsa_preprocess + qsa_forward; device-side failures are read with
+ * qsa_read_no_alloc_status. */
 QSA_API qsa_status qsa_forward_no_alloc(const qsa_problem *problem, const void *routes, const void *q, const void *k,
                                         const void *v, void *o, float *lse, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * qsa_forward_no_alloc's array on the current device (what
+ * qsa_read_device_status does for a caller workspace).  Blocks the host. */
+QSA_API qsa_status qsa_read_no_alloc_status(cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the workspace's device status
  * word: QSA_ERR_TIMEOUT if a kernel's bounded wait gave up, QSA_ERR_DEVICE_CHECK

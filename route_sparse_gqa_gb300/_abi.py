@@ -31,6 +31,7 @@ EXPORTS = (
     "qsa_backward_deterministic",
     "qsa_copy_route_sets",
     "qsa_forward_no_alloc",
+    "qsa_read_no_alloc_status",
     "qsa_read_device_status",
     "qsa_status_string",
     "qsa_last_error",
@@ -95,6 +96,7 @@ def load() -> ctypes.CDLL:
         lib.qsa_copy_route_sets.argtypes = [P, vp, sz, vp, vp, vp]
         lib.qsa_forward_no_alloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_read_device_status.argtypes = [vp, vp]
+        lib.qsa_read_no_alloc_status.argtypes = [vp]
         lib.qsa_status_string.argtypes = [ctypes.c_int]
         lib.qsa_status_string.restype = ctypes.c_char_p
         lib.qsa_last_error.argtypes = []
@@ -110,7 +112,8 @@ def load() -> ctypes.CDLL:
         lib.qsa_select_token_ids.argtypes = [R, vp, vp, vp, vp, sz, vp, vp]
         for name in ("qsa_check_problem", "qsa_preprocess", "qsa_forward", "qsa_backward",
                      "qsa_backward_deterministic", "qsa_copy_route_sets",
-                     "qsa_forward_no_alloc", "qsa_read_device_status", "qsa_route_check_problem",
+                     "qsa_forward_no_alloc", "qsa_read_no_alloc_status", "qsa_read_device_status",
+                     "qsa_route_check_problem",
                      "qsa_index_scores", "qsa_select_from_scores", "qsa_select_token_ids"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib

@@ -93,7 +93,7 @@ bool tc_head_major_order(const AttnArgs &a, int64_t n_g) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&bytes, cudaDevAttrL2CacheSize, dev);
     const int64_t l2 = bytes > 0 ? bytes : (64ll << 20);
-    const int64_t acc_bytes = a.B * a.S_kv * n_g * kHeadDim * 2 * (int64_t)sizeof(float);
+    const int64_t acc_bytes = a.B * a.S_kv * n_g * a.D * 2 * (int64_t)sizeof(float);
     return acc_bytes > l2 / 2;
 }
 

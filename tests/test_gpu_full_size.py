@@ -5,7 +5,12 @@ seconds, so:
 * route sets are compared bit for bit on EVERY row;
 * O, LSE and dQ on sampled rows (first, last, empty, random), each recomputed
   by the oracle from its own inputs;
-* dK and dV on sampled keys, recomputed from every row that routes to them;
+* dK and dV on sampled keys, recomputed from every row that routes to them:
+  keys late in the sequence (few routing rows) and the hottest ones -- the
+  first routed key (block 0, routed by thousands of rows on the long
+  workloads: the most reductions and the most work items per chunk) and the
+  last routed key (the last rows' own block; past 2^31 bytes of K/V on the
+  long-K/V workload);
 * properties that hold at any size on the whole output: sum_j dK_j = 0 and
   sum_j dV_j = sum of dO over the group's non-empty rows (fp32 accumulators),
   and exact zeros for keys no row routes to.
@@ -39,13 +44,17 @@ def _sample_rows(rng, counts_b, n):
 
 def _sample_keys(rng, ids_b, counts_b, S_kv, n, max_rows=1500):
     """Keys late in the sequence (few routing rows, so the oracle stays fast),
-    plus one never-routed key if there is one."""
+    the first and the last routed key (the hottest and the highest), plus one
+    never-routed key if there is one."""
     used = np.zeros(S_kv, bool)
     valid = ids_b[ids_b >= 0]
     used[valid] = True
     cand = np.nonzero(used)[0]
-    cand = cand[cand >= cand.max() - 512] if cand.size else cand
-    keys = np.sort(rng.choice(cand, size=min(n, cand.size), replace=False))
+    late = cand[cand >= cand.max() - 512] if cand.size else cand
+    keys = set(rng.choice(late, size=min(n, late.size), replace=False).tolist())
+    if cand.size:
+        keys.update((int(cand[0]), int(cand[-1])))
+    keys = np.array(sorted(keys), dtype=np.int64)
     unused = np.nonzero(~used)[0]
     return keys, unused
 
@@ -93,17 +102,28 @@ def test_workload_full_size(index):
             assert np.all(np.abs(dv_sum - expect) <= 1e-3 * scale_v), f"sum dV b{b} g{g}"
 
 
-def test_right_padded_workload_every_element():
+_ORACLE_CACHE = {}
+
+
+@pytest.mark.parametrize("fwd", ["auto", "keymajor"])
+def test_right_padded_workload_every_element(fwd, monkeypatch):
     """Every output element of the right-padded workload against the full oracle
-    (forward and backward, ~15 s of oracle time).  Short tiles there (two chunks)
+    (forward and backward, ~15 s of oracle time, computed once).  Short tiles there (two chunks)
     end their items right after their first PV, which exposes any barrier-phase
-    mistake between the PV and the epilogue that sampled rows can miss."""
+    mistake between the PV and the epilogue that sampled rows can miss.  Run with
+    the forward the device chooses (the tile forward here) and with the key-major
+    forward forced."""
+    if fwd != "auto":
+        monkeypatch.setenv("QSA_DEBUG_FORWARD_PATH", fwd)
     case = W.make_case(1)
     w = case.workload
     out = run_library(case.q, case.k, case.v, case.do, case.routes, w.softmax_scale, fp32_dkdv=True)
-    qd, kd, vd, dod = f64(case.q), f64(case.k), f64(case.v), f64(case.do)
-    o_ref, lse_ref = oracle.forward(qd, kd, vd, case.routes, w.softmax_scale)
-    dq_ref, dk_ref, dv_ref = oracle.backward(qd, kd, vd, case.routes, dod, w.softmax_scale)
+    if not _ORACLE_CACHE:
+        qd, kd, vd, dod = f64(case.q), f64(case.k), f64(case.v), f64(case.do)
+        _ORACLE_CACHE["fwd"] = oracle.forward(qd, kd, vd, case.routes, w.softmax_scale)
+        _ORACLE_CACHE["bwd"] = oracle.backward(qd, kd, vd, case.routes, dod, w.softmax_scale)
+    o_ref, lse_ref = _ORACLE_CACHE["fwd"]
+    dq_ref, dk_ref, dv_ref = _ORACLE_CACHE["bwd"]
     assert_close("O", out["o"], o_ref)
     assert_lse_close(out["lse"], lse_ref)
     assert_close("dQ", out["dq"], dq_ref)

@@ -4,20 +4,25 @@ It exists for callers that cannot allocate device memory while they run (code
 inside a framework that owns all device memory, such as an inference engine
 plugin's enqueue, or a latency-critical loop that cannot take an allocation's
 implicit synchronisation).  Its scratch is a fixed 32 MiB device array inside
-libqsa.  This test calls it through the C ABI twice in a row on different
-problems, so the second call runs on the array the first one left behind, and
-checks both against the allocating qsa_preprocess + qsa_forward path at the
-parity tolerances.  It also checks that an oversize problem is refused before
-any device work.  It sits in its own file so pytest collects it last.
+libqsa.  These tests call it through the C ABI on several problems in a row, so
+later calls run on the array earlier ones left behind, and check each call
+against the fp64 oracle and against the allocating qsa_preprocess +
+qsa_forward path at the parity tolerances; they cover the tile kernels (G = 8),
+the warp-level kernels (G = 3) and a ragged problem with int64 routes.  They
+also check that a warm call leaves the device's free memory unchanged, that a
+device-side failure of a call is reported by qsa_read_no_alloc_status, and that
+an oversize problem is refused before any device work.  This file sits last in
+pytest's collection order.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 from route_sparse_gqa_gb300 import _abi
 from route_sparse_gqa_gb300 import workloads as W
-from tests.qsa_testlib import assert_close, assert_lse_close, bf16_to_device
+from tests.qsa_testlib import assert_close, assert_lse_close, bf16_to_device, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -30,12 +35,15 @@ def lib():
     return _abi.load()
 
 
-def _inputs(index_or_seed):
-    if index_or_seed == 0:
+def _inputs(kind):
+    if kind == "tiny":
         c = W.make_case(0)
         return c.q, c.k, c.v, c.routes, c.workload.softmax_scale
-    rng = np.random.default_rng(index_or_seed)
-    B, S_q, S_kv, Hq, Hkv, K = 2, 75, 333, 16, 2, 90  # ragged last tile, int64 routes with huge values
+    rng = np.random.default_rng(12345 if kind == "ragged" else 777)
+    if kind == "ragged":  # G = 8, ragged last tile, int64 routes with huge values
+        B, S_q, S_kv, Hq, Hkv, K = 2, 75, 333, 16, 2, 90
+    else:  # G = 3: the warp-level kernels on the same array
+        B, S_q, S_kv, Hq, Hkv, K = 1, 40, 200, 6, 2, 30
     q = W.bf16_normal(rng, (B, S_q, Hq, 256))
     k = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
     v = W.bf16_normal(rng, (B, S_kv, Hkv, 256))
@@ -45,28 +53,86 @@ def _inputs(index_or_seed):
     return q, k, v, r, 0.07
 
 
-def test_no_alloc_forward_matches_allocating_path(lib):
+def _no_alloc(lib, plan, routes, q, k, v, o, lse):
+    import torch
+
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    p = plan.problem
+    return lib.qsa_forward_no_alloc(ctypes.byref(p), routes.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                    o.data_ptr(), lse.data_ptr(), stream)
+
+
+def test_no_alloc_forward_matches_oracle_and_allocating_path(lib):
     import torch
 
     import route_sparse_gqa_gb300 as qsa
 
     dev = torch.device("cuda:0")
-    for case in (0, 12345):  # two calls in a row on the shared scratch
-        qb, kb, vb, routes_np, scale = _inputs(case)
+    for kind in ("tiny", "ragged", "g3", "tiny"):  # calls in a row on the shared array
+        qb, kb, vb, routes_np, scale = _inputs(kind)
         q, k, v = (bf16_to_device(x, dev) for x in (qb, kb, vb))
         routes = torch.from_numpy(routes_np).to(dev)
         plan = qsa.preprocess(q, k, v, routes, scale)
         o_ref, lse_ref = qsa.forward(plan, q, k, v)
-
-        p = plan.problem
         o = torch.full_like(o_ref, float("nan"))
         lse = torch.full_like(lse_ref, float("nan"))
-        stream = torch.cuda.current_stream(dev).cuda_stream
-        _abi.check(lib.qsa_forward_no_alloc(ctypes.byref(p), routes.data_ptr(), q.data_ptr(), k.data_ptr(),
-                                            v.data_ptr(), o.data_ptr(), lse.data_ptr(), stream))
-        torch.cuda.synchronize()
-        assert_close("O", o.float().cpu().numpy().astype(np.float64), o_ref.float().cpu().numpy().astype(np.float64))
-        assert_lse_close(lse.cpu().numpy().astype(np.float64), lse_ref.cpu().numpy().astype(np.float64))
+        _abi.check(_no_alloc(lib, plan, routes, q, k, v, o, lse))
+        _abi.check(lib.qsa_read_no_alloc_status(torch.cuda.current_stream(dev).cuda_stream))
+        got_o = o.float().cpu().numpy().astype(np.float64)
+        got_lse = lse.cpu().numpy().astype(np.float64)
+        assert_close("O vs allocating path", got_o, o_ref.float().cpu().numpy().astype(np.float64))
+        assert_lse_close(got_lse, lse_ref.cpu().numpy().astype(np.float64))
+        oo, ll = oracle.forward(f64(qb), f64(kb), f64(vb), routes_np, scale)
+        assert_close("O vs oracle", got_o, oo)
+        assert_lse_close(got_lse, ll)
+
+
+def test_no_alloc_call_allocates_nothing(lib):
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    dev = torch.device("cuda:0")
+    qb, kb, vb, routes_np, scale = _inputs("ragged")
+    q, k, v = (bf16_to_device(x, dev) for x in (qb, kb, vb))
+    routes = torch.from_numpy(routes_np).to(dev)
+    plan = qsa.preprocess(q, k, v, routes, scale)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=dev)
+    _abi.check(_no_alloc(lib, plan, routes, q, k, v, o, lse))  # warm: kernels loaded, limits set
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    for _ in range(3):
+        _abi.check(_no_alloc(lib, plan, routes, q, k, v, o, lse))
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+
+
+def test_no_alloc_reports_device_failures(lib, monkeypatch):
+    """A bounded wait made to run out (the QSA_DEBUG_WAIT_LIMIT_NS=0 test hook, read at launch) is
+    reported by qsa_read_no_alloc_status, and the next call on the same context is correct again."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    dev = torch.device("cuda:0")
+    qb, kb, vb, routes_np, scale = _inputs("ragged")
+    q, k, v = (bf16_to_device(x, dev) for x in (qb, kb, vb))
+    routes = torch.from_numpy(routes_np).to(dev)
+    plan = qsa.preprocess(q, k, v, routes, scale)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    monkeypatch.setenv("QSA_DEBUG_WAIT_LIMIT_NS", "0")
+    _abi.check(_no_alloc(lib, plan, routes, q, k, v, o, lse))
+    assert lib.qsa_read_no_alloc_status(stream) == 5  # QSA_ERR_TIMEOUT
+    monkeypatch.delenv("QSA_DEBUG_WAIT_LIMIT_NS")
+    _abi.check(_no_alloc(lib, plan, routes, q, k, v, o, lse))
+    _abi.check(lib.qsa_read_no_alloc_status(stream))
+    oo, ll = oracle.forward(f64(qb), f64(kb), f64(vb), routes_np, scale)
+    assert_close("O after a reported failure", o.float().cpu().numpy().astype(np.float64), oo)
+    assert_lse_close(lse.cpu().numpy().astype(np.float64), ll)
 
 
 def test_no_alloc_rejects_oversize_problem(lib):
