@@ -597,22 +597,28 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                         break;
                     }
                     tc_fence_after();
-                    uint32_t v[4][32];
-#pragma unroll
-                    for (int b4 = 0; b4 < 4; ++b4) tmem_ld32(trow + L::kTmemO + 128 * h + b4 * 32, v[b4]);
-                    tmem_ld_wait();
-                    tc_fence_before();
-                    mbar_arrive(bars + kOOFree0 + h);
+                    // 64 rows at a time (fewer live registers); the TMEM half is released after the second read.
                     float *acc = p.o_acc + h * 128 + dl;
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int r0 = jj * 8;  // eight heads of one query
-                        const int64_t q = __shfl_sync(0xffffffffu, my_q, r0 >> gshift);
-                        if (r0 < nrows) {
-                            const int64_t off = ((it.b * p.S_q + q) * p.Hq + it.g * p.G + (r0 & gmask)) * D;
+                    for (int part = 0; part < 2; ++part) {
+                        uint32_t v[2][32];
+                        tmem_ld32(trow + L::kTmemO + 128 * h + part * 64, v[0]);
+                        tmem_ld32(trow + L::kTmemO + 128 * h + part * 64 + 32, v[1]);
+                        tmem_ld_wait();
+                        if (part == 1) {
+                            tc_fence_before();
+                            mbar_arrive(bars + kOOFree0 + h);
+                        }
 #pragma unroll
-                            for (int t = 0; t < 8; ++t)
-                                red_add_f32(acc + off + t * D, __uint_as_float(v[jj >> 2][(jj & 3) * 8 + t]));
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int r0 = part * 64 + jj * 8;  // eight heads of one query
+                            const int64_t q = __shfl_sync(0xffffffffu, my_q, r0 >> gshift);
+                            if (r0 < nrows) {
+                                const int64_t off = ((it.b * p.S_q + q) * p.Hq + it.g * p.G + (r0 & gmask)) * D;
+#pragma unroll
+                                for (int t = 0; t < 8; ++t)
+                                    red_add_f32(acc + off + t * D, __uint_as_float(v[jj >> 2][(jj & 3) * 8 + t]));
+                            }
                         }
                     }
                 }

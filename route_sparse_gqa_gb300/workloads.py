@@ -89,6 +89,10 @@ WORKLOADS = (
              "B2 S4096 Hq16 Hkv2 D128, routes as right-padded-blocks"),
     Workload(6, "right-padded-mha", 2, 4096, 4096, 16, 16, 256, 2048, np.int32, 1.0 / 16,
              "B2 S4096 Hq16 Hkv16 (G=1) D256, routes as right-padded-blocks"),
+    # A quarter-length train-step (same heads and route recipe, inputs still larger than L2): the size the
+    # many-pass counter captures run on.
+    Workload(7, "train-step-s8192", 1, 8192, 8192, 32, 4, 256, 2048, np.int32, 1.0 / 16,
+             "B1 S8192 Hq32 Hkv4 D256, int32 K=2048, 48 causal blocks clipped to 2048 IDs"),
 )
 
 _ROWS_PER_PIECE = 2048
@@ -278,7 +282,7 @@ def make_routes(w: Workload, rng: np.random.Generator) -> np.ndarray:
         pos = 98304 + np.arange(S)
         r = _block_routes(rng, pos, np.zeros(S, np.int64), 31, K)
         return r.reshape(1, S, K).astype(w.route_dtype)
-    if w.index == 4:
+    if w.index in (4, 7):
         pos = np.arange(S)
         r = _block_routes(rng, pos, np.zeros(S, np.int64), 47, K)
         return r.reshape(1, S, K).astype(w.route_dtype)
