@@ -85,6 +85,41 @@ def work_counts(w, counts: np.ndarray):
     }
 
 
+def executed_pairs(w, ids: np.ndarray, counts: np.ndarray) -> dict:
+    """Tensor-core (query-head row, key) pairs each kernel family computes per KV head, over the useful ones
+    (routed pairs x G heads).  The tile kernels compute every key of a T-query tile's union of route sets,
+    packed 64 at a time; the key-major kernels compute every key of an aligned 64-key chunk for groups of T
+    routing queries inside one query window (the window the library sizes to 32 MiB of fp32 dQ per KV head).
+    Host-side bookkeeping from the route sets; the forward's key-major max pass recomputes S once more."""
+    G = w.Hq // w.Hkv
+    T = 128 // G
+    useful = int(counts.astype(np.int64).sum()) * G
+    B, S_q, K = ids.shape
+    tile_chunks = 0
+    for b in range(B):
+        for t0 in range(0, S_q, T):
+            blk = ids[b, t0:t0 + T]
+            tile_chunks += -(-np.unique(blk[blk >= 0]).size // 64)
+    n_blk = -(-S_q // 64)
+    w_max = max(256, (32 << 20) // (G * w.D * 4))
+    n_win = -(-n_blk // (-(-w_max // 64)))
+    win_rows = -(-n_blk // n_win) * 64
+    NC = -(-w.S_kv // 64)
+    groups = 0
+    for b in range(B):
+        c = np.where(ids[b] >= 0, ids[b] // 64, -1)
+        first = np.ones_like(c, dtype=bool)
+        first[:, 1:] = c[:, 1:] != c[:, :-1]
+        keep = first & (c >= 0)
+        win = np.broadcast_to((np.arange(S_q) // win_rows)[:, None], c.shape)
+        n = np.bincount((win[keep].astype(np.int64) * NC + c[keep]), minlength=n_win * NC)
+        groups += int((-(-n // T)).sum())
+    tile = tile_chunks * 64 * 128
+    km = groups * 64 * 128
+    return {"tile_over_useful": round(tile / max(useful, 1), 3), "keymajor_over_useful": round(km / max(useful, 1), 3),
+            "tile_chunks": int(tile_chunks), "keymajor_groups": groups}
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -240,9 +275,11 @@ def time_attention(args, index, dev, qsa, flush, world, sample_clocks):
         return plan, o, lse, dq, dk, dv
 
     plan, *_ = step()
-    _, counts = plan.route_sets()
+    ids, counts = plan.route_sets()
     plan.device_status()
     wc = work_counts(w, counts.cpu().numpy())
+    pairs = executed_pairs(w, ids.cpu().numpy(), counts.cpu().numpy())
+    del ids
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -299,6 +336,7 @@ def time_attention(args, index, dev, qsa, flush, world, sample_clocks):
         "bwd_tflops": round(bwd_tf, 2),
         "fwd_frac": round(fwd_tf / tc_peak, 4),
         "bwd_frac": round(bwd_tf / tc_peak, 4),
+        "executed_pairs": pairs,
         "gathered_bytes": {
             "note": "per-row K/V gather model (no reuse); DRAM traffic is far lower, so fractions exceed 1",
             "fwd_gbs": round(fwd_gbs, 1),
@@ -385,10 +423,12 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-# libqsa kernels per step on the headline workload: preprocess = route rows + route tiles + tile order,
-# forward = 1, backward = delta + 7 reverse-list kernels (masks, column scan, two scans, fill, items,
-# queue) + the key-major kernel + dQ conversion + dK/dV conversion.
-LAUNCHES_PER_STEP = 3 + 1 + 11
+# libqsa kernels per step on the headline workload.  Preprocess: route rows, route tiles, tile order, the
+# 7 reverse-list kernels (masks, column scan, two scans, fill, items, queue) and the path choice = 11.
+# Forward: the tile forward (returns at once when the key-major forward is chosen) + the key-major forward's key norms,
+# init, row-max pass (returns at once when every row's bound serves), output pass and final division = 6.  Backward: delta, the key-major kernel, dQ conversion,
+# dK/dV conversion = 4.
+LAUNCHES_PER_STEP = 11 + 6 + 4
 
 
 def pipelined_e2e(dev, host: dict, outs: dict, compute_fn, n: int, n_slots: int) -> float:

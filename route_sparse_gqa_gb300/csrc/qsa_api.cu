@@ -140,12 +140,17 @@ Layout make_layout(const qsa_problem *p) {
         off = align256(off + (size_t)(L.cap_items * p->Hkv) * sizeof(int32_t));
         L.off_kmeta = off;  // {entries, items, queue length, overflow, forward path choice, -, tile chunks, groups}
         off = align256(off + 8 * sizeof(int32_t));
-        // Key-major forward: row maxima and sums, and the fp32 accumulator it shares with the backward's dQ
-        // (8 bytes per element for the deterministic backward's exact sums).
+        // Key-major forward: row maxima, exponent references and sums, the key norm bound, and the fp32
+        // accumulator it shares with the backward's dQ (8 bytes per element for the deterministic
+        // backward's exact sums).
         L.off_mrow = off;
         off = align256(off + (size_t)(p->B * p->Hq * p->S_q) * sizeof(int32_t));
-        L.off_lrow = off;
+        L.off_mref = off;
         off = align256(off + (size_t)(p->B * p->Hq * p->S_q) * sizeof(float));
+        L.off_lrow = off;
+        off = align256(off + (size_t)(p->B * p->Hq * p->S_q) * 2 * sizeof(float));
+        L.off_kbound = off;
+        off = align256(off + (size_t)(kKeyNormWord + p->B * p->Hkv) * sizeof(int32_t));
         L.off_dq = off;
         off = align256(off + (size_t)rows * p->Hq * p->D * 8);
     }
@@ -269,6 +274,7 @@ ChunkArgs chunk_args(const qsa_problem *p, const Layout &L, void *ws) {
     c.sorted = at<int32_t>(ws, L.off_sorted);
     c.queue = at<int32_t>(ws, L.off_queue);
     c.meta = at<int32_t>(ws, L.off_kmeta);
+    c.status = at<DeviceStatus>(ws, L.off_status);
     return c;
 }
 
@@ -505,7 +511,9 @@ qsa_status qsa_forward(const qsa_problem *p, void *ws, size_t ws_bytes, const vo
             k.e_mask = at<uint64_t>(ws, L.off_emask);
             k.sched = at<int32_t>(ws, L.off_sched) + 6;
             k.mrow = at<int32_t>(ws, L.off_mrow);
+            k.mref = at<float>(ws, L.off_mref);
             k.lrow = at<float>(ws, L.off_lrow);
+            k.kbound = at<int32_t>(ws, L.off_kbound);
             k.o_acc = at<float>(ws, L.off_dq);
             k.choice = choice;
             e = launch_km_forward(a, k, static_cast<__nv_bfloat16 *>(o), lse, stream);

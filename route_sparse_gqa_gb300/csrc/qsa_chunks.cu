@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(kQueueThreads) chunk_queue_kernel(ChunkArgs a)
         if (threadIdx.x == 0) {
             a.meta[2] = 0;
             a.meta[3] = 1;
+            raise_status(a.status, QSA_ERR_DEVICE_CHECK, kSiteChunkCapacity, (unsigned)n_items, (unsigned)a.cap_items);
         }
         return;
     }

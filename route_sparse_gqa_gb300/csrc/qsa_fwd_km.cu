@@ -73,12 +73,23 @@ struct KfParams {
     const int32_t *e_q;
     const uint64_t *e_mask;
     int32_t *sched;   // work queue counters {next, done}
-    int32_t *mrow;    // [B, Hq, S_q] encoded row maximum (log2 units)
-    float *lrow;      // [B, Hq, S_q] sum of exp2(s - max)
+    // Row statistics, [B, S_q, Hq] (a query's heads adjacent, so one warp's reductions share sectors).
+    int32_t *mrow;    // encoded row maximum of s * sl2 (row-max pass only)
+    float *mref;      // the exponent reference of the bound (used when *need_max == 0)
+    // Pairs {sum of P = exp2(s * sl2 - reference), sum of P rounded to BF16}: the first gives the LSE, the
+    // second normalises O, whose numerator sums the same rounded P (so a row's weights add up to one and a
+    // row with one routed key returns that key's value exactly).
+    float *lrow;
     float *o_acc;     // [B, S_q, Hq, D] fp32
-    const int32_t *choice;  // 1: this forward runs
+    const int32_t *choice;    // 1: this forward runs
+    const int32_t *need_max;  // 1: some row's bound is too loose, the row-max pass runs
     DeviceStatus *status;
 };
+
+// The exponent reference of row `stat`: the bound, or the exact maximum when the row-max pass ran.
+__device__ __forceinline__ float row_reference(const KfParams &p, bool need_max, int64_t stat) {
+    return need_max ? dec_max(__ldg(p.mrow + stat)) : __ldg(p.mref + stat);
+}
 
 struct KfItem {
     int64_t b, g, c;
@@ -145,7 +156,8 @@ struct MaxLayout {
 
 template <int D>
 __global__ void __launch_bounds__(kMaxThreads, 1) km_fwd_max_kernel(const __grid_constant__ KfParams p) {
-    if (*p.choice != 1) return;  // the tile forward runs instead (uniform over the grid)
+    // The tile forward runs instead, or every row's bound serves as its reference (uniform over the grid).
+    if (*p.choice != 1 || *p.need_max == 0) return;
     using L = MaxLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -310,7 +322,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) km_fwd_max_kernel(const __grid
 #pragma unroll
                 for (int j = 0; j < 64; ++j)
                     if ((mask >> j) & 1ull) mx = fmaxf(mx, __uint_as_float(sr[j >> 5][j & 31]) * p.sl2);
-                if (mask) red_max_s32(p.mrow + (it.b * p.Hq + h) * p.S_q + q, enc_max(mx));
+                if (mask) red_max_s32(p.mrow + (it.b * p.S_q + q) * p.Hq + h, enc_max(mx));
             }
         }
         if (!ok) fail(5);
@@ -517,6 +529,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
         const int r = threadIdx.x;
         const int slot = (int)(r / p.G), hl = (int)(r % p.G);
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const bool need_max = *p.need_max != 0;
         int64_t gc = 0;
         KfItem it;
         bool ok = true;
@@ -532,8 +545,8 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                 const bool live = e < it.e0 + it.ne;
                 const uint64_t mask = live ? __ldg(p.e_mask + e) : 0ull;
                 const int64_t q = live ? __ldg(p.e_q + e) : 0;
-                const int64_t stat = (it.b * p.Hq + h) * p.S_q + q;
-                const float m2 = mask ? dec_max(__ldg(p.mrow + stat)) : 0.f;
+                const int64_t stat = (it.b * p.S_q + q) * p.Hq + h;
+                const float m2 = mask ? row_reference(p, need_max, stat) : 0.f;
                 if (!waitw(kOSFull0 + sb, ring_parity<2>(gc))) {
                     ok = false;
                     break;
@@ -546,7 +559,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                 tc_fence_before();
                 mbar_arrive(bars + kOSFree0 + sb);
                 uint32_t pk[32];
-                float lsum = 0.f;
+                float lsum = 0.f, lsum_b = 0.f;
 #pragma unroll
                 for (int j = 0; j < 64; j += 2) {
                     const float p0 = ((mask >> j) & 1ull) ? ex2(__uint_as_float(sr[j >> 5][j & 31]) * p.sl2 - m2) : 0.f;
@@ -554,7 +567,9 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                                          ? ex2(__uint_as_float(sr[(j + 1) >> 5][(j + 1) & 31]) * p.sl2 - m2)
                                          : 0.f;
                     lsum += p0 + p1;
-                    pk[j >> 1] = pack_bf16(p0, p1);
+                    const uint32_t w = pack_bf16(p0, p1);
+                    lsum_b += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+                    pk[j >> 1] = w;
                 }
                 if (gc >= 2 && !waitw(kOPFree0 + sb, ring_parity<2>(gc - 2))) {
                     ok = false;
@@ -568,7 +583,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bars + kOPFull0 + sb);
-                if (mask) red_add_f32(p.lrow + stat, lsum);
+                if (mask) red_add_v2_f32(p.lrow + 2 * stat, lsum, lsum_b);
             }
         }
         if (!ok) fail(5);
@@ -635,16 +650,95 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
 
 // ---------------------------------------------------------------------------------------------------
 // Accumulator set-up and the final division.
-__global__ void km_fwd_init_kernel(KfParams p, int64_t n_stat, int64_t n_o4) {
+// Exponent references without a row-max pass.  By Cauchy-Schwarz every score of row (q, h) satisfies
+// s * sl2 <= |sl2| |q_h| max_j |k_j,g| =: m_ref, so P = exp2(s sl2 - m_ref) <= 1 (no overflow, as with
+// the exact maximum).  The row's maximum is at least the score s0 of any one routed key (its first one
+// here), so m_ref - s0 bounds how far the largest P falls below 1.  While that gap is at most
+// kMaxRefGap = 64 for every row, the largest P of a row is >= 2^-64: terms that fall below fp32's normal
+// range (2^-126) change l by less than K 2^-62 relative, and products flushed in the tensor core change
+// O by less than K 2^-62 absolute, far below the BF16 rounding of the outputs; the results equal those
+// with the exact maximum up to rounding.  A row with a wider gap sets *need_max and the row-max pass
+// computes exact maxima for all rows.
+constexpr float kMaxRefGap = 64.f;
+
+// Largest squared key norm per (batch row, KV head) over all keys (one atomicMax per CTA and head on the
+// float bits, which order as unsigned integers for non-negative values).
+__global__ void __launch_bounds__(256) km_key_norm_kernel(AttnArgs a, const int32_t *choice, unsigned *kmax2) {
+    if (*choice != 1) return;
+    __shared__ unsigned smax[64];
+    const int lane = threadIdx.x & 31;
+    const int64_t Hkv = a.Hkv, nb = a.B * Hkv;
+    for (int i = threadIdx.x; i < nb && i < 64; i += blockDim.x) smax[i] = 0u;
+    __syncthreads();
+    const int64_t n_rows = a.B * a.S_kv * Hkv;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < n_rows; row += warps) {
+        const int64_t g = row % Hkv, bj = row / Hkv;
+        const int64_t b = bj / a.S_kv, j = bj % a.S_kv;
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (lane * 8 < a.D)
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.k + b * a.ks0 + j * a.ks1 + g * a.ks2 + lane * 8), f);
+        float n2 = 0.f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) n2 = fmaf(f[t], f[t], n2);
+        n2 = warp_sum(n2);
+        if (lane == 0) {
+            const int64_t bg = b * Hkv + g;
+            if (nb <= 64) atomicMax(&smax[bg], __float_as_uint(n2));
+            else atomicMax(kmax2 + bg, __float_as_uint(n2));
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb && nb <= 64; i += blockDim.x)
+        if (smax[i]) atomicMax(kmax2 + i, smax[i]);
+}
+
+// Zeroes the accumulators and the row sums, resets the row maxima, and writes each row's reference
+// (one warp per (b, q, h) row: |q_h| and the score of the row's first routed key).
+__global__ void __launch_bounds__(256) km_fwd_init_kernel(KfParams p, AttnArgs a, const int32_t *ids,
+                                                          const int32_t *counts, int64_t K,
+                                                          const unsigned *kmax2, int force_max,
+                                                          int32_t *need_max, int64_t n_o4) {
     if (*p.choice != 1) return;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_stat; i += stride) {
-        p.mrow[i] = kEncNegInf;
-        p.lrow[i] = 0.f;
-    }
     float4 *o4 = reinterpret_cast<float4 *>(p.o_acc);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_o4; i += stride)
         o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (force_max && blockIdx.x == 0 && threadIdx.x == 0) *need_max = 1;
+    const int lane = threadIdx.x & 31;
+    const int64_t n_stat = p.B * p.S_q * p.Hq;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const float asl2 = fabsf(p.sl2);
+    for (int64_t stat = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); stat < n_stat;
+         stat += warps) {
+        const int64_t h = stat % p.Hq, bq = stat / p.Hq;
+        const int64_t b = bq / p.S_q, q = bq % p.S_q;
+        const int64_t g = h / p.G;
+        const int32_t cnt = __ldg(counts + bq);
+        float qf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, kf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (cnt > 0 && lane * 8 < a.D) {
+            const int64_t j0 = __ldg(ids + bq * K);
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.q + b * a.qs0 + q * a.qs1 + h * a.qs2 + lane * 8), qf);
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.k + b * a.ks0 + j0 * a.ks1 + g * a.ks2 + lane * 8), kf);
+        }
+        float n2 = 0.f, dot = 0.f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            n2 = fmaf(qf[t], qf[t], n2);
+            dot = fmaf(qf[t], kf[t], dot);
+        }
+        n2 = warp_sum(n2);
+        dot = warp_sum(dot);
+        if (lane == 0) {
+            // Rounded up by 2^-10 relative: covers the fp32 rounding of the norms and of the tensor-core dot
+            // products (each far below 2^-16 relative of |q| |k|).
+            const float mref = asl2 * sqrtf(n2) * sqrtf(__uint_as_float(kmax2[b * p.Hkv + g])) * (1.f + 1.f / 1024.f);
+            p.mref[stat] = mref;
+            p.mrow[stat] = kEncNegInf;
+            reinterpret_cast<float2 *>(p.lrow)[stat] = make_float2(0.f, 0.f);
+            if (cnt > 0 && !(mref - dot * p.sl2 <= kMaxRefGap)) *need_max = 1;  // also catches NaN / inf
+        }
+    }
 }
 
 // O = acc / l as BF16 (zero for rows without routes), LSE = (max + log2 l) ln 2 (natural log, -inf for
@@ -659,14 +753,17 @@ __global__ void km_fwd_final_kernel(KfParams p, __nv_bfloat16 *o, float *lse) {
         const int64_t row = i / kPer;
         const int64_t h = row % p.Hq, bq = row / p.Hq;
         const int64_t b = bq / p.S_q, q = bq % p.S_q;
-        const int64_t stat = (b * p.Hq + h) * p.S_q + q;
-        const float l = p.lrow[stat];
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int64_t stat = row;  // [B, S_q, Hq]
+        const float2 ls = reinterpret_cast<const float2 *>(p.lrow)[stat];
+        const float l = ls.x;
+        const float inv = ls.y > 0.f ? 1.f / ls.y : 0.f;
         const float4 *a4 = reinterpret_cast<const float4 *>(p.o_acc) + 2 * i;
         const float4 x = a4[0], y = a4[1];
         const float f[8] = {x.x * inv, x.y * inv, x.z * inv, x.w * inv, y.x * inv, y.y * inv, y.z * inv, y.w * inv};
         reinterpret_cast<uint4 *>(o)[i] = f32x8_to_bf16(f);
-        if (i % kPer == 0) lse[stat] = l > 0.f ? (dec_max(p.mrow[stat]) + __log2f(l)) * kLn2 : -INFINITY;
+        if (i % kPer == 0)
+            lse[(b * p.Hq + h) * p.S_q + q] = l > 0.f ? (row_reference(p, *p.need_max != 0, stat) + __log2f(l)) * kLn2
+                                                       : -INFINITY;
     }
 }
 
@@ -773,18 +870,26 @@ cudaError_t launch_km_forward(const AttnArgs &a, const KfArgs &k, __nv_bfloat16 
     p.e_q = k.e_q;
     p.e_mask = k.e_mask;
     p.mrow = k.mrow;
+    p.mref = k.mref;
     p.lrow = k.lrow;
     p.o_acc = k.o_acc;
     p.choice = k.choice;
+    p.need_max = k.kbound;
     p.status = a.status;
     const int sms = tc_num_sms();
-    const int64_t n_stat = a.B * a.Hq * a.S_q;
     const int64_t n_o4 = a.B * a.S_q * a.Hq * D / 4;
-    km_fwd_init_kernel<<<sms * 8, 256, 0, s>>>(p, n_stat, n_o4);
+    // kbound = {need_max, -, ..., squared key norm maxima from word kKeyNormWord}: cleared, then filled.
+    unsigned *kmax2 = reinterpret_cast<unsigned *>(k.kbound + kKeyNormWord);
+    cudaError_t e = cudaMemsetAsync(k.kbound, 0, (kKeyNormWord + a.B * a.Hkv) * sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
+    km_key_norm_kernel<<<sms * 4, 256, 0, s>>>(a, k.choice, kmax2);
+    const char *force = std::getenv("QSA_DEBUG_FORWARD_MAXPASS");
+    km_fwd_init_kernel<<<sms * 8, 256, 0, s>>>(p, a, a.ids, a.counts, a.K, kmax2, force && force[0] == '1', k.kbound,
+                                                n_o4);
     p.sched = k.sched;
     if (D == 128) km_fwd_max_kernel<128><<<sms, kMaxThreads, MaxLayout<128>::kSmemBytes, s>>>(p);
     else km_fwd_max_kernel<256><<<sms, kMaxThreads, MaxLayout<256>::kSmemBytes, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.sched = k.sched + 2;
     if (D == 128) km_fwd_out_kernel<128><<<sms, kOutThreads, OutLayout<128>::kSmemBytes, s>>>(p);

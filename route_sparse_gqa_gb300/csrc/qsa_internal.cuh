@@ -34,7 +34,7 @@ struct Layout {
     bool km;
     int64_t NC, n_blk_b, win_blocks, n_win_b, max_groups, cap_entries, cap_items;
     size_t off_rmask, off_hoff, off_list_start, off_eq, off_emask, off_part_start, off_items, off_sorted, off_queue, off_kmeta;
-    size_t off_mrow, off_lrow;  // key-major forward row statistics
+    size_t off_mrow, off_mref, off_lrow, off_kbound;  // key-major forward row statistics and key norm bound
     size_t off_delta, off_dk, off_dv, off_dq, total;  // off_dk/off_dv/off_dq: 8 bytes per element (fp32 or fixed point)
 };
 
@@ -52,6 +52,7 @@ enum Site : unsigned int {
     kSiteTileBwdKey = 21,
     kSiteKeyBwdWait = 22,
     kSiteKeyFwdWait = 23,
+    kSiteChunkCapacity = 24,
     kSiteRouteScoreWait = 30,
 };
 
@@ -142,6 +143,7 @@ struct ChunkArgs {
     int32_t *sorted;      // [cap_items]: items by window, largest first
     int32_t *queue;       // [cap_items * Hkv]: item * Hkv + KV head, in work order
     int32_t *meta;        // {entries, items, queue length, overflow flag}
+    DeviceStatus *status;  // raised (QSA_ERR_DEVICE_CHECK) if a capacity would be exceeded
 };
 cudaError_t launch_chunk_lists(const ChunkArgs &a, cudaStream_t s);
 

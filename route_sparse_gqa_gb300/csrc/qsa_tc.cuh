@@ -88,11 +88,14 @@ struct KfArgs {
     const int32_t *queue, *meta, *e_q;
     const uint64_t *e_mask;
     int32_t *sched;   // two pairs of work queue counters {next, done}: row-max pass, output pass
-    int32_t *mrow;    // [B, Hq, S_q]
-    float *lrow;      // [B, Hq, S_q]
+    int32_t *mrow;    // [B, S_q, Hq] encoded row maxima
+    float *mref;      // [B, S_q, Hq] exponent references from the norm bound
+    float *lrow;      // [B, S_q, Hq] pairs: sums of P and of P rounded to BF16
     float *o_acc;     // [B, S_q, Hq, D] fp32
     const int32_t *choice;
+    int32_t *kbound;  // [kKeyNormWord + B * Hkv]: {row-max pass needed, ...}, then squared key norm maxima
 };
+constexpr int64_t kKeyNormWord = 64;
 bool km_forward_shape_ok(const AttnArgs &a);
 int forced_path(const char *env_var);  // debug override of a path choice: 0 tile, 1 key-major, -1 none
 cudaError_t launch_km_choose(const int32_t *tile_nchunks, int64_t n_tiles, const int32_t *list_start,

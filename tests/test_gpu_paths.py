@@ -86,3 +86,31 @@ def test_keymajor_forward_deterministic_backward(monkeypatch):
     assert_close("dQ", runs[0]["dq"], dq_ref)
     assert_close("dK", runs[0]["dk"], dk_ref)
     assert_close("dV", runs[0]["dv"], dv_ref)
+
+
+@pytest.mark.parametrize("mode", ["bound", "forced-max", "large-logits"])
+def test_keymajor_forward_reference(mode, monkeypatch):
+    """The key-major forward's exponent reference: the Cauchy-Schwarz bound (unit-variance inputs keep every
+    row's gap well under the limit), the row-max pass forced by the test hook QSA_DEBUG_FORWARD_MAXPASS, and
+    queries scaled by 4 (exact in BF16), whose logits spread beyond the bound's limit so the row-max
+    pass runs on its own."""
+    monkeypatch.setenv("QSA_DEBUG_FORWARD_PATH", "keymajor")
+    if mode == "forced-max":
+        monkeypatch.setenv("QSA_DEBUG_FORWARD_MAXPASS", "1")
+    q, k, v, do, routes = _case(77, 1, 180, 350, 16, 2, 120, 256, "blocks", np.int32)
+    if mode == "large-logits":
+        q = W.bf16_bits_from_f32(W.bf16_bits_to_f32(q) * np.float32(4.0))
+    scale = 1.0 / 16
+    out = run_library(q, k, v, do, routes, scale, fp32_dkdv=True)
+    qd, kd, vd, dod = f64(q), f64(k), f64(v), f64(do)
+    o_ref, lse_ref = oracle.forward(qd, kd, vd, routes, scale)
+    assert_close("O", out["o"], o_ref)
+    assert_lse_close(out["lse"], lse_ref)
+    if mode == "large-logits":
+        # Forward only: the backward's Delta = <dO, O> reads the BF16 output, and with logits this sharp
+        # that rounding alone moves dK past the parity tolerance (whichever forward made O).
+        return
+    dq_ref, dk_ref, dv_ref = oracle.backward(qd, kd, vd, routes, dod, scale)
+    assert_close("dQ", out["dq"], dq_ref)
+    assert_close("dK", out["dk"], dk_ref)
+    assert_close("dV", out["dv"], dv_ref)
