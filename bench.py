@@ -423,12 +423,13 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-# libqsa kernels per step on the headline workload.  Preprocess: route rows, route tiles, tile order, the
-# 7 reverse-list kernels (masks, column scan, two scans, fill, items, queue) and the path choice = 11.
-# Forward: the tile forward (returns at once when the key-major forward is chosen) + the key-major forward's key norms,
-# init, row-max pass (returns at once when every row's bound serves), output pass and final division = 6.  Backward: delta, the key-major kernel, dQ conversion,
-# dK/dV conversion = 4.
-LAUNCHES_PER_STEP = 11 + 6 + 4
+# libqsa kernels per step on the headline workload.  Preprocess: route rows, the 7 reverse-list kernels
+# (masks, column scan, two scans, fill, items, queue), the path choice, route tiles and tile order (both
+# return at once when the key-major kernels run both ways) = 11.  Forward: the tile forward (returns at once)
+# + the key-major forward's key norms, init, row-max pass (returns at once when every row's bound serves),
+# output pass and final division = 6.  Backward: delta, the tile backward (returns at once), the key-major
+# kernel, dQ conversion, dK/dV conversion = 5.
+LAUNCHES_PER_STEP = 11 + 6 + 5
 
 
 def pipelined_e2e(dev, host: dict, outs: dict, compute_fn, n: int, n_slots: int) -> float:

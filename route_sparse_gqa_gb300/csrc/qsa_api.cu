@@ -113,7 +113,9 @@ Layout make_layout(const qsa_problem *p) {
         L.cap_entries = rows * std::min<int64_t>(p->K, L.NC);
         L.cap_items = L.cap_entries / (L.max_groups * L.T) + p->B * L.NC * L.n_win_b + 1;
         const int64_t n_win = p->B * L.n_win_b;
-        L.km = L.NC <= kKmMaxChunks && p->B * L.n_blk_b * L.NC <= kKmMaskWords && L.cap_entries < INT32_MAX &&
+        // (The key-major kernels take G = 8..64; with the lists in place the tile lists are built only for the
+        // tile forward, so a problem outside that range must not get them.)
+        L.km = L.G >= 8 && L.G <= 64 && L.NC <= kKmMaxChunks && p->B * L.n_blk_b * L.NC <= kKmMaskWords && L.cap_entries < INT32_MAX &&
                L.cap_items * p->Hkv < INT32_MAX && n_win <= kKmMaxWindows &&
                n_win * (L.max_groups + 1) <= kKmQueueBins && p->B * L.NC < INT32_MAX && rows * p->Hq < INT32_MAX;
     }
@@ -140,6 +142,8 @@ Layout make_layout(const qsa_problem *p) {
         off = align256(off + (size_t)(L.cap_items * p->Hkv) * sizeof(int32_t));
         L.off_kmeta = off;  // {entries, items, queue length, overflow, forward path choice, -, tile chunks, groups}
         off = align256(off + 8 * sizeof(int32_t));
+        L.off_tkeys = off;  // distinct routed keys per query tile (the tile forward's cost, for the path choice)
+        off = align256(off + (size_t)(p->B * L.n_tiles) * sizeof(int32_t));
         // Key-major forward: row maxima, exponent references and sums, the key norm bound, and the fp32
         // accumulator it shares with the backward's dQ (8 bytes per element for the deterministic
         // backward's exact sums).
@@ -274,6 +278,7 @@ ChunkArgs chunk_args(const qsa_problem *p, const Layout &L, void *ws) {
     c.sorted = at<int32_t>(ws, L.off_sorted);
     c.queue = at<int32_t>(ws, L.off_queue);
     c.meta = at<int32_t>(ws, L.off_kmeta);
+    c.tile_keys = at<int32_t>(ws, L.off_tkeys);
     c.status = at<DeviceStatus>(ws, L.off_status);
     return c;
 }
@@ -346,8 +351,12 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
     b.dv = static_cast<__nv_bfloat16 *>(dv);
     const size_t n_kv = (size_t)p->B * p->S_kv * p->Hkv * p->D;
     const size_t n_q = (size_t)p->B * p->S_q * p->Hq * p->D;
-    const bool key_major = L.km && tc_backward_supported() && km_backward_shape_ok(b.f) &&
-                           forced_path("QSA_DEBUG_BACKWARD_PATH") != 0;
+    // With reverse lists both backward kernels are launched (when the tile one accepts the problem) and the
+    // device-side choice made at preprocessing (choice[1], test hooks included) lets one of them run.
+    const bool key_major = L.km && tc_backward_supported() && km_backward_shape_ok(b.f);
+    const TileArgs ta = tile_args(p, L, ws);
+    const bool tile_ok = L.T && tc_backward_supported() && tc_backward_shape_ok(b.f, ta);
+    const int32_t *bwd_choice = at<int32_t>(ws, L.off_kmeta) + 5;
     cudaError_t e;
     if (deterministic) {
         // Fixed-point accumulators in the workspace; the caller's fp32 buffers (if any) receive the sums.
@@ -386,12 +395,16 @@ qsa_status backward_impl(const qsa_problem *p, void *ws, size_t ws_bytes, const 
         } else {
             k.dq_acc = at<float>(ws, L.off_dq);
         }
+        k.gate = tile_ok ? bwd_choice : nullptr;
+        if (tile_ok) {
+            e = launch_tc_backward(b, ta, bwd_choice, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
+        }
         e = launch_km_backward(b, k, stream);
         if (e != cudaSuccess) return cuda_fail(e, "key-major backward launch");
     } else {
-        const TileArgs ta = tile_args(p, L, ws);
-        if (L.T && tc_backward_supported() && tc_backward_shape_ok(b.f, ta)) {
-            e = launch_tc_backward(b, ta, stream);
+        if (tile_ok) {
+            e = launch_tc_backward(b, ta, nullptr, stream);
             if (e != cudaSuccess) return cuda_fail(e, "tile backward launch");
         } else {
             e = launch_rowwise_backward(b, stream);
@@ -440,6 +453,19 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
     r.counts = at<int32_t>(ws, L.off_counts);
     e = launch_route_rows(r, stream);
     if (e != cudaSuccess) return cuda_fail(e, "route_rows launch");
+    const int32_t *choice = nullptr;
+    if (L.km) {
+        // Reverse lists for the key-major kernels, and the forward path choice.
+        const ChunkArgs c = chunk_args(p, L, ws);
+        e = launch_chunk_lists(c, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "reverse route list launch");
+        const AttnArgs a = attn_args(p, L, ws, nullptr, nullptr, nullptr);
+        const bool tile_bwd_ok = tc_backward_supported() && tc_backward_shape_ok(a, tile_args(p, L, ws));
+        e = launch_km_choose(c.tile_keys, p->B * L.n_tiles, c.list_start, p->B * L.NC, L.T, p->D, tile_bwd_ok,
+                             c.meta + 4, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "path choice launch");
+        choice = c.meta + 4;
+    }
     if (L.T) {
         TilesArgs t{};
         t.B = p->B;
@@ -456,17 +482,10 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
         t.tile_keys = at<int32_t>(ws, L.off_tile_keys);
         t.tile_masks = at<uint64_t>(ws, L.off_tile_masks);
         t.order = at<int32_t>(ws, L.off_order);
+        // With reverse lists the tile lists are built only if the device chose a tile kernel in either direction.
+        t.skip = choice;
         e = launch_route_tiles(t, stream);
         if (e != cudaSuccess) return cuda_fail(e, "route_tiles launch");
-    }
-    if (L.km) {
-        // Reverse lists for the key-major kernels, and the forward path choice.
-        const ChunkArgs c = chunk_args(p, L, ws);
-        e = launch_chunk_lists(c, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "reverse route list launch");
-        e = launch_km_choose(at<int32_t>(ws, L.off_tile_nchunks), p->B * L.n_tiles, c.list_start, p->B * L.NC, L.T,
-                             c.meta + 4, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "path choice launch");
     }
     return QSA_OK;
 }

@@ -114,6 +114,7 @@ struct KmParams {
     const float *lse, *delta;
     float *dq_acc, *dk_acc, *dv_acc;
     FxAcc dq_fx, dk_fx, dv_fx;
+    const int32_t *gate;  // null, or a device flag: the kernel returns at once when *gate == 0 (tile runs)
     DeviceStatus *status;
 };
 
@@ -137,6 +138,7 @@ __device__ __forceinline__ void km_decode(const KmParams &p, int32_t idx, KmItem
 
 template <int D, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1) km_bwd_kernel(const __grid_constant__ KmParams p) {
+    if (p.gate && *p.gate == 0) return;  // the tile backward runs instead (uniform over the grid)
     using L = KmLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -593,7 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1) km_bwd_kernel(const __grid_consta
 
 // fp32 dQ accumulator (or the exact pair est/lo) -> BF16 dQ.
 template <bool kDet>
-__global__ void dq_convert_kernel(const float *acc, FxAcc fx, __nv_bfloat16 *dq, int64_t n8) {
+__global__ void dq_convert_kernel(const float *acc, FxAcc fx, __nv_bfloat16 *dq, int64_t n8, const int32_t *gate) {
+    if (gate && *gate == 0) return;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
         float f[8];
         if (kDet) {
@@ -680,6 +683,7 @@ cudaError_t launch_km_backward(const BwdArgs &bw, const KmArgs &k, cudaStream_t 
     p.dv_acc = bw.dv_acc;
     p.dk_fx = bw.dk_fx;
     p.dv_fx = bw.dv_fx;
+    p.gate = k.gate;
     p.status = a.status;
     const int grid = tc_num_sms();
     const bool det = bw.dk_fx.est != nullptr;
@@ -695,8 +699,8 @@ cudaError_t launch_km_backward(const BwdArgs &bw, const KmArgs &k, cudaStream_t 
     const int64_t n8 = a.B * a.S_q * a.Hq * D / 8;
     const int64_t nb = (n8 + 255) / 256;
     const int blocks = (int)std::min<int64_t>(nb, (int64_t)tc_num_sms() * 16);
-    if (det) dq_convert_kernel<true><<<blocks, 256, 0, s>>>(nullptr, k.dq_fx, bw.dq, n8);
-    else dq_convert_kernel<false><<<blocks, 256, 0, s>>>(k.dq_acc, FxAcc{}, bw.dq, n8);
+    if (det) dq_convert_kernel<true><<<blocks, 256, 0, s>>>(nullptr, k.dq_fx, bw.dq, n8, k.gate);
+    else dq_convert_kernel<false><<<blocks, 256, 0, s>>>(k.dq_acc, FxAcc{}, bw.dq, n8, k.gate);
     return cudaGetLastError();
 }
 

@@ -95,6 +95,7 @@ struct BwdParams {
     __nv_bfloat16 *dq;
     float *dk_acc, *dv_acc;
     FxAcc dk_fx, dv_fx;  // deterministic mode: exact accumulators
+    const int32_t *gate;  // null, or a device flag: the kernel returns at once when *gate == 1 (key-major runs)
     DeviceStatus *status;
 };
 
@@ -111,6 +112,7 @@ enum BarId {
 // reproducible sums).
 template <int D, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
+    if (p.gate && *p.gate == 1) return;  // the key-major backward runs instead (uniform over the grid)
     using L = BwdLayout<D>;
     constexpr uint32_t kOffQ = L::kOffQ, kOffDO = L::kOffDO, kOffK = L::kOffK, kOffV = L::kOffV;
     constexpr uint32_t kOffP = L::kOffP, kOffDS = L::kOffDS, kOffBar = L::kOffBar, kOffMisc = L::kOffMisc;
@@ -549,7 +551,7 @@ bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t) {
     return t.T >= 2 && t.T * a.G == kTileRows && a.B <= kMaxPairs && (a.D == 256 || a.D == 128);
 }
 
-cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_t s) {
+cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, const int32_t *gate, cudaStream_t s) {
     const AttnArgs &a = bw.f;
     const int64_t D = a.D;
     BwdParams p;
@@ -588,6 +590,7 @@ cudaError_t launch_tc_backward(const BwdArgs &bw, const TileArgs &t, cudaStream_
     p.dv_acc = bw.dv_acc;
     p.dk_fx = bw.dk_fx;
     p.dv_fx = bw.dv_fx;
+    p.gate = gate;
     p.status = a.status;
     for (int64_t g0 = 0; g0 < a.Hkv; g0 += g_per_launch) {
         const int64_t n_g = std::min<int64_t>(g_per_launch, a.Hkv - g0);

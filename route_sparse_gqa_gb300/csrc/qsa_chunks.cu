@@ -66,59 +66,84 @@ __device__ __forceinline__ int block_scan_excl(int x, int *warp_tot, int &total)
 constexpr int kBlockRows = 64;     // query rows per block (one 64-bit row mask)
 constexpr int kBlockThreads = 1024;  // 32 warps: two rows of the block each
 
-// Walks the sorted ids of row r (of the block) 32 at a time and calls
-// emit(c, m) once per chunk c the row routes into, with m the mask of the
-// chunk keys it routes to (lane-parallel: at the lane that ends the chunk's run
-// of ids; a run that continues into the next 32 ids is carried there).  kMask:
-// whether m is needed (segmented OR over the run's lanes).
+// Walks the sorted ids of one row and calls emit(c, m) once per chunk c the row
+// routes into, with m the mask of the chunk keys it routes to (kMask; 0
+// otherwise).  Lane L takes a contiguous range of ceil(n / 32) ids and walks it
+// alone, so a run of ids in one chunk costs a compare and an OR per id; runs
+// that cross lane boundaries (a chunk's ids split between neighbouring lanes,
+// or spanning several lanes of a short row) are joined with one segmented scan
+// over the lanes, and emitted by the lane where they end.
 template <bool kMask, typename F>
 __device__ __forceinline__ void walk_row_chunks(const int32_t *ids, int n, int lane, F &&emit) {
-    int carry_c = -1;
-    uint64_t carry_m = 0;
-    constexpr int kAhead = 4;  // 32-id batches loaded together (independent loads in flight)
-    for (int base0 = 0; base0 < n; base0 += 32 * kAhead) {
-        int32_t idv[kAhead];
+    if (n <= 0) return;
+    const int per = (n + 31) >> 5;
+    const int i0 = min(n, lane * per), i1 = min(n, i0 + per);
+    int cf = -1, cl = -1;   // chunks of the lane's first and last runs
+    uint64_t mf = 0, ml = 0;  // their key masks
+    int nruns = 0;
+    constexpr int kBatch = 8;  // ids loaded together (independent loads in flight)
+    for (int base = i0; base < i1; base += kBatch) {
+        int32_t buf[kBatch];
 #pragma unroll
-        for (int u = 0; u < kAhead; ++u) {
-            const int i = base0 + 32 * u + lane;
-            idv[u] = i < n ? __ldg(ids + i) : 0;
-        }
+        for (int u = 0; u < kBatch; ++u) buf[u] = base + u < i1 ? __ldg(ids + base + u) : 0;
 #pragma unroll
-        for (int u = 0; u < kAhead; ++u) {
-            const int base = base0 + 32 * u;
-            if (base >= n) break;
-            const int i = base + lane;
-            const bool valid = i < n;
-            const int32_t id = idv[u];
-            const int c = valid ? (id >> 6) : -1;
-            uint64_t m = 0;
-            if (kMask) {
-                m = valid ? (1ull << (id & 63)) : 0ull;
-                // Segmented inclusive OR: the lanes of one chunk are contiguous (ids ascend).
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint64_t y = __shfl_up_sync(0xffffffffu, m, o);
-                    const int cy = __shfl_up_sync(0xffffffffu, c, o);
-                    if (lane >= o && cy == c) m |= y;
+        for (int u = 0; u < kBatch; ++u) {
+            if (base + u >= i1) break;
+            const int c = buf[u] >> 6;
+            if (c != cl) {
+                if (nruns == 1) {
+                    cf = cl;
+                    mf = ml;
+                } else if (nruns > 1) {
+                    emit(cl, ml);  // a run that starts and ends inside this lane's range
                 }
-                if (valid && c == carry_c) m |= carry_m;  // the carried run continues here
+                cl = c;
+                ml = 0;
+                ++nruns;
             }
-            const int c0 = __shfl_sync(0xffffffffu, c, 0);
-            // The carried run ended with the previous 32 ids: emit it (its chunk differs from all below).
-            if (carry_c >= 0 && c0 != carry_c && lane == 0) emit(carry_c, carry_m);
-            const int c_next = __shfl_down_sync(0xffffffffu, c, 1);
-            const int n_here = n - base < 32 ? n - base : 32;
-            const bool last_lane = lane == n_here - 1;
-            const bool more = base + 32 < n;
-            if (valid && (last_lane || c_next != c) && !(last_lane && more)) emit(c, m);
-            carry_c = more ? __shfl_sync(0xffffffffu, c, 31) : -1;
-            carry_m = more ? __shfl_sync(0xffffffffu, m, 31) : 0ull;
+            if (kMask) ml |= 1ull << (buf[u] & 63);
         }
+    }
+    if (nruns == 1) {
+        cf = cl;
+        mf = ml;
+    }
+    const bool single = nruns == 1;
+    // Whether the first run continues the previous lane's last run, and whether the next lane's first run
+    // continues this lane's last run (empty lanes have cf = cl = -1 and continue nothing).
+    const int cl_prev = __shfl_up_sync(0xffffffffu, cl, 1);
+    const int cf_next = __shfl_down_sync(0xffffffffu, cf, 1);
+    const bool cont_in = nruns > 0 && lane > 0 && cf == cl_prev;
+    const bool cont_out = nruns > 0 && lane < 31 && cf_next >= 0 && cf_next == cl;
+    uint64_t carry = 0;  // mask of the run this lane's first run continues, over the lanes before it
+    if (kMask) {
+        // Segmented inclusive OR over the lanes' last runs: a lane whose whole range is one run that continues
+        // the previous lane's links to it; any other lane starts a segment.
+        uint64_t acc = ml;
+        bool head = !(single && cont_in);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t up = __shfl_up_sync(0xffffffffu, acc, o);
+            const bool head_up = __shfl_up_sync(0xffffffffu, head, o);
+            if (lane >= o && !head) {
+                acc |= up;
+                head = head_up;
+            }
+        }
+        const uint64_t prev = __shfl_up_sync(0xffffffffu, acc, 1);
+        carry = cont_in ? prev : 0ull;
+    }
+    if (nruns == 0) return;
+    if (single) {
+        if (!cont_out) emit(cf, mf | carry);
+    } else {
+        emit(cf, mf | carry);
+        if (!cont_out) emit(cl, ml);
     }
 }
 
 // One CTA per block of 64 query rows: rmask[block][c] = the block's rows that route into chunk c.
-__global__ void __launch_bounds__(kBlockThreads) chunk_mask_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(kBlockThreads, 2) chunk_mask_kernel(ChunkArgs a) {
     extern __shared__ unsigned long long tbl[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int64_t blk = blockIdx.x;
@@ -195,6 +220,35 @@ __global__ void __launch_bounds__(kBlockThreads) chunk_fill_kernel(ChunkArgs a) 
             a.e_q[pos] = (int32_t)(q0 + r);
             a.e_mask[pos] = m;
         });
+    }
+    if (!a.tile_keys) return;
+    // The block's query tiles (T = slots rows each): distinct routed keys per tile, the union of its rows'
+    // masks summed over the chunks.  The block's entries of chunk c are contiguous in list c and in row
+    // order, so each tile's rows form one run there.
+    int *tcount = reinterpret_cast<int *>(base + a.NC);
+    const int tiles = (kBlockRows + (int)a.slots - 1) / (int)a.slots;
+    for (int t = threadIdx.x; t < tiles; t += blockDim.x) tcount[t] = 0;
+    __syncthreads();  // also makes the entries written above visible to the whole block
+    for (int64_t c = threadIdx.x; c < a.NC; c += blockDim.x) {
+        const int n = __popcll(tbl[c]);
+        int cur = -1;
+        uint64_t u = 0;
+        for (int i = 0; i < n; ++i) {
+            const int t = (int)((a.e_q[base[c] + i] - q0) / a.slots);
+            if (t != cur) {
+                if (cur >= 0) atomicAdd(&tcount[cur], __popcll(u));
+                cur = t;
+                u = 0;
+            }
+            u |= a.e_mask[base[c] + i];
+        }
+        if (cur >= 0) atomicAdd(&tcount[cur], __popcll(u));
+    }
+    __syncthreads();
+    const int64_t n_tiles_b = (a.S_q + a.slots - 1) / a.slots;
+    for (int t = threadIdx.x; t < tiles; t += blockDim.x) {
+        const int64_t tg = q0 / a.slots + t;
+        if (tg < n_tiles_b) a.tile_keys[b * n_tiles_b + tg] = tcount[t];
     }
 }
 
@@ -314,7 +368,7 @@ __global__ void __launch_bounds__(kQueueThreads) chunk_queue_kernel(ChunkArgs a)
 cudaError_t launch_chunk_lists(const ChunkArgs &a, cudaStream_t s) {
     const int64_t n_blk = a.B * a.n_blk_b, n_lists = a.B * a.NC;
     const size_t smem_mask = (size_t)a.NC * sizeof(uint64_t);
-    const size_t smem_fill = (size_t)a.NC * (sizeof(uint64_t) + sizeof(int32_t));
+    const size_t smem_fill = (size_t)a.NC * (sizeof(uint64_t) + sizeof(int32_t)) + kBlockRows * sizeof(int32_t);
     cudaError_t e = cudaSuccess;
     if (smem_fill > 48 * 1024) {
         e = cudaFuncSetAttribute(chunk_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_mask);

@@ -785,18 +785,20 @@ cudaError_t set_km_fwd_smem() {
 }
 
 // One CTA: which forward runs, from the work each path would do.  The tile path computes every (row, key)
-// pair of its tiles' chunk unions, one chunk of T queries per unit; the key-major path computes only routed
+// pair of its tiles' chunk unions, one chunk of T queries per unit (a tile's distinct routed keys packed 64
+// to a chunk); the key-major path computes only routed
 // pairs, one group of T queries per unit, but reduces its outputs through L2, so a group costs about as
 // much as kFwdRatio tile chunks.  choice[2], choice[3]: the two unit counts (saturated), for inspection.
 constexpr int kFwdRatioNum = 3, kFwdRatioDen = 1;
-__global__ void __launch_bounds__(1024) km_choose_kernel(const int32_t *tile_nchunks, int64_t n_tiles,
+__global__ void __launch_bounds__(1024) km_choose_kernel(const int32_t *tile_keys, int64_t n_tiles,
                                                          const int32_t *list_start, int64_t n_lists, int64_t slots,
-                                                         int force_fwd, int32_t *choice) {
+                                                         int force_fwd, int force_bwd, int bwd_num, int bwd_den,
+                                                         int32_t *choice) {
     __shared__ unsigned long long tot[2];
     if (threadIdx.x == 0) tot[0] = tot[1] = 0ull;
     __syncthreads();
     unsigned long long a = 0, g = 0;
-    for (int64_t i = threadIdx.x; i < n_tiles; i += blockDim.x) a += (unsigned long long)tile_nchunks[i];
+    for (int64_t i = threadIdx.x; i < n_tiles; i += blockDim.x) a += (unsigned long long)((tile_keys[i] + 63) / 64);
     for (int64_t i = threadIdx.x; i < n_lists; i += blockDim.x)
         g += (unsigned long long)((list_start[i + 1] - list_start[i] + slots - 1) / slots);
     atomicAdd(&tot[0], a);
@@ -805,8 +807,9 @@ __global__ void __launch_bounds__(1024) km_choose_kernel(const int32_t *tile_nch
     if (threadIdx.x == 0) {
         const unsigned long long chunks = tot[0], groups = tot[1];
         const int fwd = n_tiles == 0 ? 1 : (groups * kFwdRatioNum < chunks * kFwdRatioDen ? 1 : 0);
+        const int bwd = n_tiles == 0 || bwd_den == 0 ? 1 : (groups * bwd_num < chunks * bwd_den ? 1 : 0);
         choice[0] = force_fwd >= 0 ? force_fwd : fwd;
-        choice[1] = 0;
+        choice[1] = bwd_den == 0 ? 1 : force_bwd >= 0 ? force_bwd : bwd;
         choice[2] = (int32_t)(chunks < 0x7FFFFFFFull ? chunks : 0x7FFFFFFFull);
         choice[3] = (int32_t)(groups < 0x7FFFFFFFull ? groups : 0x7FFFFFFFull);
     }
@@ -829,10 +832,15 @@ bool km_forward_shape_ok(const AttnArgs &a) {
     return pow2 && a.G >= 8 && a.G <= 64 && (a.D == 256 || a.D == 128);
 }
 
-cudaError_t launch_km_choose(const int32_t *tile_nchunks, int64_t n_tiles, const int32_t *list_start,
-                             int64_t n_lists, int64_t slots, int32_t *choice, cudaStream_t s) {
-    km_choose_kernel<<<1, 1024, 0, s>>>(tile_nchunks, n_tiles, list_start, n_lists, slots,
-                                        forced_path("QSA_DEBUG_FORWARD_PATH"), choice);
+cudaError_t launch_km_choose(const int32_t *tile_keys, int64_t n_tiles, const int32_t *list_start,
+                             int64_t n_lists, int64_t slots, int64_t D, bool tile_bwd_ok, int32_t *choice,
+                             cudaStream_t s) {
+    // Backward: a key-major group costs about kBwdRatio tile chunks (per unit and KV head: tile 33-34 ns and
+    // key-major 35-41 ns at D = 256 on train-step and right-padded; 24 against 32 ns at D = 128).
+    const int bwd_num = D == 128 ? 27 : 6, bwd_den = tile_bwd_ok ? (D == 128 ? 20 : 5) : 0;
+    km_choose_kernel<<<1, 1024, 0, s>>>(tile_keys, n_tiles, list_start, n_lists, slots,
+                                        forced_path("QSA_DEBUG_FORWARD_PATH"), forced_path("QSA_DEBUG_BACKWARD_PATH"),
+                                        bwd_num, bwd_den, choice);
     return cudaGetLastError();
 }
 

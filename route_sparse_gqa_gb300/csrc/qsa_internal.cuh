@@ -33,7 +33,8 @@ struct Layout {
     // Key-major paths (qsa_chunks.cu, qsa_fwd_km.cu, qsa_bwd_km.cu); km = false when the problem does not take them.
     bool km;
     int64_t NC, n_blk_b, win_blocks, n_win_b, max_groups, cap_entries, cap_items;
-    size_t off_rmask, off_hoff, off_list_start, off_eq, off_emask, off_part_start, off_items, off_sorted, off_queue, off_kmeta;
+    size_t off_rmask, off_hoff, off_list_start, off_eq, off_emask, off_part_start, off_items, off_sorted, off_queue, off_kmeta,
+        off_tkeys;
     size_t off_mrow, off_mref, off_lrow, off_kbound;  // key-major forward row statistics and key norm bound
     size_t off_delta, off_dk, off_dv, off_dq, total;  // off_dk/off_dv/off_dq: 8 bytes per element (fp32 or fixed point)
 };
@@ -112,6 +113,7 @@ struct TilesArgs {
     int32_t *tile_keys;       // [B*n_tiles, max_chunks*64]
     uint64_t *tile_masks;     // [B*n_tiles, max_chunks, T]
     int32_t *order;           // [B*n_tiles*Hkv] work items, heaviest first
+    const int32_t *skip;      // if set and skip[0] == skip[1] == 1 (key-major forward and backward), nothing is built
 };
 cudaError_t launch_route_tiles(const TilesArgs &a, cudaStream_t s);
 
@@ -143,6 +145,7 @@ struct ChunkArgs {
     int32_t *sorted;      // [cap_items]: items by window, largest first
     int32_t *queue;       // [cap_items * Hkv]: item * Hkv + KV head, in work order
     int32_t *meta;        // {entries, items, queue length, overflow flag}
+    int32_t *tile_keys;   // [B * ceil(S_q / slots)]: distinct routed keys of each query tile (null: not needed)
     DeviceStatus *status;  // raised (QSA_ERR_DEVICE_CHECK) if a capacity would be exceeded
 };
 cudaError_t launch_chunk_lists(const ChunkArgs &a, cudaStream_t s);

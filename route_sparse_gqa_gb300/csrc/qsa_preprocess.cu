@@ -309,6 +309,7 @@ __device__ __forceinline__ void emit_chunk(const TilesArgs &a, int64_t tile, int
 }
 
 __global__ void __launch_bounds__(kTileThreads) route_tiles_kernel(TilesArgs a) {
+    if (a.skip && a.skip[0] == 1 && a.skip[1] == 1) return;
     extern __shared__ uint32_t tsm[];
     uint32_t *mem = tsm;                                              // [W] per-key query bitmask
     uint32_t *cw = mem + kTileWindow;                                 // [W + 64] compacted bitmasks
@@ -426,7 +427,9 @@ constexpr int kOrderThreads = 1024;
 constexpr int kOrderBins = 8192;
 
 // Tiles sorted by chunk count, heaviest first (counting sort; ties in any order).
-__global__ void __launch_bounds__(kOrderThreads) route_order_kernel(const int32_t *nchunks, int64_t n, int32_t *order) {
+__global__ void __launch_bounds__(kOrderThreads) route_order_kernel(const int32_t *nchunks, int64_t n, int32_t *order,
+                                                                    const int32_t *skip) {
+    if (skip && skip[0] == 1 && skip[1] == 1) return;
     __shared__ int hist[kOrderBins];
     __shared__ int warp_tot[33];
     for (int i = threadIdx.x; i < kOrderBins; i += blockDim.x) hist[i] = 0;
@@ -472,7 +475,7 @@ cudaError_t launch_route_tiles(const TilesArgs &a, cudaStream_t s) {
     route_tiles_kernel<<<(unsigned)tiles, kTileThreads, smem, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    route_order_kernel<<<1, kOrderThreads, 0, s>>>(a.tile_nchunks, tiles, a.order);
+    route_order_kernel<<<1, kOrderThreads, 0, s>>>(a.tile_nchunks, tiles, a.order, a.skip);
     return cudaGetLastError();
 }
 

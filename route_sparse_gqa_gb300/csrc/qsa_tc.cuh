@@ -75,6 +75,7 @@ struct KmArgs {
     int32_t *sched;  // work queue counters {next, done}
     float *dq_acc;   // fp32 [B, S_q, Hq, D] (zeroed), or null in deterministic mode
     FxAcc dq_fx;     // deterministic mode: exact accumulators
+    const int32_t *gate;  // null, or a device flag: the kernel and its dQ conversion run only when *gate == 1
 };
 bool km_backward_shape_ok(const AttnArgs &a);
 cudaError_t launch_km_backward(const BwdArgs &b, const KmArgs &k, cudaStream_t s);
@@ -98,12 +99,15 @@ struct KfArgs {
 constexpr int64_t kKeyNormWord = 64;
 bool km_forward_shape_ok(const AttnArgs &a);
 int forced_path(const char *env_var);  // debug override of a path choice: 0 tile, 1 key-major, -1 none
-cudaError_t launch_km_choose(const int32_t *tile_nchunks, int64_t n_tiles, const int32_t *list_start,
-                             int64_t n_lists, int64_t slots, int32_t *choice, cudaStream_t s);
+// choice[0]: 1 = key-major forward; choice[1]: 1 = key-major backward (always 1 when !tile_bwd_ok).
+cudaError_t launch_km_choose(const int32_t *tile_keys, int64_t n_tiles, const int32_t *list_start,
+                             int64_t n_lists, int64_t slots, int64_t D, bool tile_bwd_ok, int32_t *choice,
+                             cudaStream_t s);
 cudaError_t launch_km_forward(const AttnArgs &a, const KfArgs &k, __nv_bfloat16 *o, float *lse, cudaStream_t s);
 
 bool tc_backward_supported();
 bool tc_backward_shape_ok(const AttnArgs &a, const TileArgs &t);
-cudaError_t launch_tc_backward(const BwdArgs &b, const TileArgs &t, cudaStream_t s);
+// gate: null, or a device flag; the tile backward returns at once when *gate == 1 (the key-major one runs).
+cudaError_t launch_tc_backward(const BwdArgs &b, const TileArgs &t, const int32_t *gate, cudaStream_t s);
 
 }  // namespace qsa
