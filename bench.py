@@ -178,7 +178,8 @@ class ClockSampler:
 # Sources each profiled kernel is built from: a recorded DRAM traffic figure stays
 # valid until one of them changes.
 KERNEL_SOURCES = {
-    "qsa_forward": ["qsa_fwd_tc.cu", "qsa_tc_host.cu", "qsa_tc_ptx.cuh", "qsa_queue.cuh", "qsa_tc.cuh", "qsa_internal.cuh"],
+    "qsa_forward": ["qsa_fwd_tc.cu", "qsa_fwd_km.cu", "qsa_tc_host.cu", "qsa_tc_ptx.cuh", "qsa_queue.cuh", "qsa_tc.cuh",
+                    "qsa_internal.cuh"],
     "qsa_backward": ["qsa_bwd_km.cu", "qsa_chunks.cu", "qsa_bwd_tc.cu", "qsa_tc_host.cu", "qsa_tc_ptx.cuh",
                      "qsa_queue.cuh", "qsa_tc.cuh", "qsa_internal.cuh"],
     "index_score_kernel": ["qsa_route.cu", "qsa_tc_host.cu", "qsa_tc_ptx.cuh", "qsa_queue.cuh", "qsa_tc.cuh",

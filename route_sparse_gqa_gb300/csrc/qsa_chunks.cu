@@ -73,19 +73,32 @@ constexpr int kBlockThreads = 1024;  // 32 warps: two rows of the block each
 // that cross lane boundaries (a chunk's ids split between neighbouring lanes,
 // or spanning several lanes of a short row) are joined with one segmented scan
 // over the lanes, and emitted by the lane where they end.
+// vec4: the row's ids start 16-byte aligned and the row has room up to a multiple of 4 ids past n, so
+// lane ranges start at multiples of 4 and are read as int4.
 template <bool kMask, typename F>
-__device__ __forceinline__ void walk_row_chunks(const int32_t *ids, int n, int lane, F &&emit) {
+__device__ __forceinline__ void walk_row_chunks(const int32_t *ids, int n, int lane, bool vec4, F &&emit) {
     if (n <= 0) return;
-    const int per = (n + 31) >> 5;
+    const int per = vec4 ? (((n + 31) >> 5) + 3) & ~3 : (n + 31) >> 5;
     const int i0 = min(n, lane * per), i1 = min(n, i0 + per);
     int cf = -1, cl = -1;   // chunks of the lane's first and last runs
     uint64_t mf = 0, ml = 0;  // their key masks
     int nruns = 0;
-    constexpr int kBatch = 8;  // ids loaded together (independent loads in flight)
+    constexpr int kBatch = 16;  // ids loaded together (independent loads in flight)
     for (int base = i0; base < i1; base += kBatch) {
         int32_t buf[kBatch];
+        if (vec4) {
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) buf[u] = base + u < i1 ? __ldg(ids + base + u) : 0;
+            for (int u = 0; u < kBatch; u += 4) {
+                const int4 v = base + u < i1 ? __ldg(reinterpret_cast<const int4 *>(ids + base + u)) : make_int4(0, 0, 0, 0);
+                buf[u] = v.x;
+                buf[u + 1] = v.y;
+                buf[u + 2] = v.z;
+                buf[u + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) buf[u] = base + u < i1 ? __ldg(ids + base + u) : 0;
+        }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             if (base + u >= i1) break;
@@ -143,7 +156,7 @@ __device__ __forceinline__ void walk_row_chunks(const int32_t *ids, int n, int l
 }
 
 // One CTA per block of 64 query rows: rmask[block][c] = the block's rows that route into chunk c.
-__global__ void __launch_bounds__(kBlockThreads, 2) chunk_mask_kernel(ChunkArgs a) {
+__global__ void __launch_bounds__(kBlockThreads) chunk_mask_kernel(ChunkArgs a) {
     extern __shared__ unsigned long long tbl[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int64_t blk = blockIdx.x;
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chunk_mask_kernel(ChunkArgs 
     for (int r = warp; r < kBlockRows && q0 + r < a.S_q; r += nwarps) {
         const int64_t row = b * a.S_q + q0 + r;
         const unsigned long long bit = 1ull << r;
-        walk_row_chunks<false>(a.ids + row * a.K, a.counts[row], lane,
+        walk_row_chunks<false>(a.ids + row * a.K, a.counts[row], lane, (a.K & 3) == 0,
                                [&](int c, uint64_t) { atomicOr(&tbl[c], bit); });
     }
     __syncthreads();
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(kBlockThreads) chunk_fill_kernel(ChunkArgs a) 
     for (int r = warp; r < kBlockRows && q0 + r < a.S_q; r += nwarps) {
         const int64_t row = b * a.S_q + q0 + r;
         const unsigned long long below = (1ull << r) - 1ull;
-        walk_row_chunks<true>(a.ids + row * a.K, a.counts[row], lane, [&](int c, uint64_t m) {
+        walk_row_chunks<true>(a.ids + row * a.K, a.counts[row], lane, (a.K & 3) == 0, [&](int c, uint64_t m) {
             const int pos = base[c] + __popcll(tbl[c] & below);
             a.e_q[pos] = (int32_t)(q0 + r);
             a.e_mask[pos] = m;
@@ -233,14 +246,26 @@ __global__ void __launch_bounds__(kBlockThreads) chunk_fill_kernel(ChunkArgs a) 
         const int n = __popcll(tbl[c]);
         int cur = -1;
         uint64_t u = 0;
-        for (int i = 0; i < n; ++i) {
-            const int t = (int)((a.e_q[base[c] + i] - q0) / a.slots);
-            if (t != cur) {
-                if (cur >= 0) atomicAdd(&tcount[cur], __popcll(u));
-                cur = t;
-                u = 0;
+        constexpr int kBatch = 4;  // entries loaded together
+        for (int i0 = 0; i0 < n; i0 += kBatch) {
+            int32_t qv[kBatch];
+            uint64_t mv[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                qv[j] = i0 + j < n ? a.e_q[base[c] + i0 + j] : 0;
+                mv[j] = i0 + j < n ? a.e_mask[base[c] + i0 + j] : 0ull;
             }
-            u |= a.e_mask[base[c] + i];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (i0 + j >= n) break;
+                const int t = (int)((qv[j] - q0) / a.slots);
+                if (t != cur) {
+                    if (cur >= 0) atomicAdd(&tcount[cur], __popcll(u));
+                    cur = t;
+                    u = 0;
+                }
+                u |= mv[j];
+            }
         }
         if (cur >= 0) atomicAdd(&tcount[cur], __popcll(u));
     }

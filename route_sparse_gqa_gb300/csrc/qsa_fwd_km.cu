@@ -338,8 +338,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) km_fwd_max_kernel(const __grid
 // half); warp 8: producer; warp 9: MMA (lane 0).  S is issued two groups ahead of O^T within an item.
 constexpr int kOutThreads = 320;
 enum OutBar { kOKVFull, kOKVFree, kOQFull0, kOQFree0 = kOQFull0 + 2, kOSFull0 = kOQFree0 + 2, kOSFree0 = kOSFull0 + 2,
-              kOPFull0 = kOSFree0 + 2, kOPFree0 = kOPFull0 + 2, kOOReady0 = kOPFree0 + 2, kOOFree0 = kOOReady0 + 2,
-              kODrain = kOOFree0 + 2, kONumFixed };
+              kOPFull0 = kOSFree0 + 2, kOPFree0 = kOPFull0 + 2, kOOReady0 = kOPFree0 + 2, kOOFree0 = kOOReady0 + 3,
+              kODrain = kOOFree0 + 3, kONumFixed };
+// O^T is produced in units of one 128-row half of D for one group (u = group * D/128 + half), each in one
+// of three 128-column TMEM slots (u mod 3), so the MMA can fill the next unit while the flush still reads
+// the two before it.
+constexpr int kOSlots = 3;
 constexpr uint32_t kOItemFull = kONumFixed, kOItemEmpty = kOItemFull + kQueueRing, kONumBars = kOItemEmpty + kQueueRing;
 
 template <int D>
@@ -355,8 +359,8 @@ struct OutLayout {
     static constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
     static constexpr uint32_t kOffMisc = kOffBar + kONumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;
-    static constexpr uint32_t kTmemO = 0;            // O^T half h at 128 h
-    static constexpr uint32_t kTmemS = 128 * kHalves;  // two S buffers of 64 columns
+    static constexpr uint32_t kTmemO = 0;                // O^T slot s at 128 s
+    static constexpr uint32_t kTmemS = 128 * kOSlots;    // two S buffers of 64 columns
 };
 
 template <int D>
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
     if (threadIdx.x == 0) {
         for (int i = 0; i < kONumFixed; ++i) {
             const bool many = (i >= kOSFree0 && i < kOSFree0 + 2) || (i >= kOPFull0 && i < kOPFull0 + 2) ||
-                              (i >= kOOFree0 && i < kOOFree0 + 2);
+                              (i >= kOOFree0 && i < kOOFree0 + kOSlots);
             mbar_init(bars + i, many ? 128u : 1u);
         }
         for (int i = 0; i < kQueueRing; ++i) {
@@ -482,7 +486,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                 mma_commit(bars + kOQFree0 + st);
                 return true;
             };
-            int64_t ic = 0, gc = 0;
+            int64_t ic = 0, gc = 0, u = 0;
             KfItem it;
             bool ok = true;
             for (int64_t pos = 0; ok; ++pos) {
@@ -497,18 +501,19 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                     const int64_t g = gc + grp;
                     const int pb = ring_slot<2>(g);
                     ok = w1(kOPFull0 + pb, ring_parity<2>(g));
-                    for (int h = 0; ok && h < L::kHalves; ++h) {
-                        // The flush has read this half of the previous group's O^T.
-                        ok = g == 0 || w1(kOOFree0 + h, (uint32_t)((g - 1) & 1));
+                    for (int h = 0; ok && h < L::kHalves; ++h, ++u) {
+                        // The flush has read the slot's previous unit.
+                        const int sl = ring_slot<kOSlots>(u);
+                        ok = u < kOSlots || w1(kOOFree0 + sl, ring_parity<kOSlots>(u - kOSlots));
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
                         for (int k = 0; k < kChunkKeys / 16; ++k)
-                            mma_bf16(tmem + L::kTmemO + 128 * h,
+                            mma_bf16(tmem + L::kTmemO + 128 * sl,
                                      sdesc_sw128(sbase + L::kOffV + (2 * h) * kKVPanel + k * 2048, kKVPanel, 1024),
                                      sdesc_sw128(sbase + L::kOffP + pb * kPBytes + k * 32, 16, 1024), idesc_o,
                                      k ? 1u : 0u);
-                        mma_commit(bars + kOOReady0 + h);
+                        mma_commit(bars + kOOReady0 + sl);
                     }
                     if (!ok) break;
                     mma_commit(bars + kOPFree0 + pb);
@@ -593,7 +598,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
         const int dl = quarter * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
         const int gshift = __ffsll(p.G) - 1, gmask = (int)p.G - 1;  // G is a power of two, at least 8
-        int64_t gc = 0;
+        int64_t gc = 0, u = 0;
         KfItem it;
         bool ok = true;
         for (int64_t pos = 0; ok; ++pos) {
@@ -606,8 +611,9 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                 const int nv = min((int32_t)p.T, it.e0 + it.ne - e0);
                 const int nrows = nv * (int)p.G;
                 const int32_t my_q = lane < nv ? __ldg(p.e_q + e0 + lane) : 0;  // lane s: slot s's query
-                for (int h = 0; h < L::kHalves; ++h) {
-                    if (!waitw(kOOReady0 + h, (uint32_t)(gc & 1))) {
+                for (int h = 0; h < L::kHalves; ++h, ++u) {
+                    const int sl = ring_slot<kOSlots>(u);
+                    if (!waitw(kOOReady0 + sl, ring_parity<kOSlots>(u))) {
                         ok = false;
                         break;
                     }
@@ -617,12 +623,12 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         uint32_t v[2][32];
-                        tmem_ld32(trow + L::kTmemO + 128 * h + part * 64, v[0]);
-                        tmem_ld32(trow + L::kTmemO + 128 * h + part * 64 + 32, v[1]);
+                        tmem_ld32(trow + L::kTmemO + 128 * sl + part * 64, v[0]);
+                        tmem_ld32(trow + L::kTmemO + 128 * sl + part * 64 + 32, v[1]);
                         tmem_ld_wait();
                         if (part == 1) {
                             tc_fence_before();
-                            mbar_arrive(bars + kOOFree0 + h);
+                            mbar_arrive(bars + kOOFree0 + sl);
                         }
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) {
@@ -801,8 +807,15 @@ __global__ void __launch_bounds__(1024) km_choose_kernel(const int32_t *tile_key
     for (int64_t i = threadIdx.x; i < n_tiles; i += blockDim.x) a += (unsigned long long)((tile_keys[i] + 63) / 64);
     for (int64_t i = threadIdx.x; i < n_lists; i += blockDim.x)
         g += (unsigned long long)((list_start[i + 1] - list_start[i] + slots - 1) / slots);
-    atomicAdd(&tot[0], a);
-    atomicAdd(&tot[1], g);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        g += __shfl_xor_sync(0xffffffffu, g, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&tot[0], a);
+        atomicAdd(&tot[1], g);
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         const unsigned long long chunks = tot[0], groups = tot[1];
