@@ -699,8 +699,9 @@ __global__ void __launch_bounds__(256) km_key_norm_kernel(AttnArgs a, const int3
         if (smax[i]) atomicMax(kmax2 + i, smax[i]);
 }
 
-// Zeroes the accumulators and the row sums, resets the row maxima, and writes each row's reference
-// (one warp per (b, q, h) row: |q_h| and the score of the row's first routed key).
+// Zeroes the accumulators and the row sums, resets the row maxima, and writes each row's reference: one
+// warp per (b, q) and eight heads of one KV head (their Q rows and the key row of the query's first routed
+// key are loaded together; lane l holds elements 8l..8l+7).
 __global__ void __launch_bounds__(256) km_fwd_init_kernel(KfParams p, AttnArgs a, const int32_t *ids,
                                                           const int32_t *counts, int64_t K,
                                                           const unsigned *kmax2, int force_max,
@@ -712,64 +713,92 @@ __global__ void __launch_bounds__(256) km_fwd_init_kernel(KfParams p, AttnArgs a
         o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (force_max && blockIdx.x == 0 && threadIdx.x == 0) *need_max = 1;
     const int lane = threadIdx.x & 31;
-    const int64_t n_stat = p.B * p.S_q * p.Hq;
+    const int64_t h8n = p.Hq / 8;  // eight-head groups per query (G is a multiple of 8)
+    const int64_t n_task = p.B * p.S_q * h8n;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const float asl2 = fabsf(p.sl2);
-    for (int64_t stat = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); stat < n_stat;
-         stat += warps) {
-        const int64_t h = stat % p.Hq, bq = stat / p.Hq;
+    const bool on = lane * 8 < a.D;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_task; t += warps) {
+        const int64_t bq = t / h8n, h0 = (t % h8n) * 8;
         const int64_t b = bq / p.S_q, q = bq % p.S_q;
-        const int64_t g = h / p.G;
+        const int64_t g = h0 / p.G;
         const int32_t cnt = __ldg(counts + bq);
-        float qf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, kf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (cnt > 0 && lane * 8 < a.D) {
-            const int64_t j0 = __ldg(ids + bq * K);
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.q + b * a.qs0 + q * a.qs1 + h * a.qs2 + lane * 8), qf);
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(a.k + b * a.ks0 + j0 * a.ks1 + g * a.ks2 + lane * 8), kf);
-        }
-        float n2 = 0.f, dot = 0.f;
+        const int32_t j0 = __ldg(ids + bq * K);
+        uint4 qv[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            n2 = fmaf(qf[t], qf[t], n2);
-            dot = fmaf(qf[t], kf[t], dot);
+        for (int j = 0; j < 8; ++j)
+            qv[j] = on && cnt > 0 ? __ldg(reinterpret_cast<const uint4 *>(a.q + b * a.qs0 + q * a.qs1 + (h0 + j) * a.qs2) + lane)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+        float kf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (on && cnt > 0)
+            bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(a.k + b * a.ks0 + (int64_t)j0 * a.ks1 + g * a.ks2) + lane), kf);
+        float n2[8], dot[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float qf[8];
+            bf16x8_to_f32(qv[j], qf);
+            n2[j] = 0.f;
+            dot[j] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                n2[j] = fmaf(qf[e], qf[e], n2[j]);
+                dot[j] = fmaf(qf[e], kf[e], dot[j]);
+            }
         }
-        n2 = warp_sum(n2);
-        dot = warp_sum(dot);
-        if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            n2[j] = warp_sum(n2[j]);
+            dot[j] = warp_sum(dot[j]);
+        }
+        if (lane < 8) {
+            float nj = 0.f, dj = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j == lane) {
+                    nj = n2[j];
+                    dj = dot[j];
+                }
+            const int64_t stat = bq * p.Hq + h0 + lane;
             // Rounded up by 2^-10 relative: covers the fp32 rounding of the norms and of the tensor-core dot
             // products (each far below 2^-16 relative of |q| |k|).
-            const float mref = asl2 * sqrtf(n2) * sqrtf(__uint_as_float(kmax2[b * p.Hkv + g])) * (1.f + 1.f / 1024.f);
+            const float mref = asl2 * sqrtf(nj) * sqrtf(__uint_as_float(kmax2[b * p.Hkv + g])) * (1.f + 1.f / 1024.f);
             p.mref[stat] = mref;
             p.mrow[stat] = kEncNegInf;
             reinterpret_cast<float2 *>(p.lrow)[stat] = make_float2(0.f, 0.f);
-            if (cnt > 0 && !(mref - dot * p.sl2 <= kMaxRefGap)) *need_max = 1;  // also catches NaN / inf
+            if (cnt > 0 && !(mref - dj * p.sl2 <= kMaxRefGap)) *need_max = 1;  // also catches NaN / inf
         }
     }
 }
 
-// O = acc / l as BF16 (zero for rows without routes), LSE = (max + log2 l) ln 2 (natural log, -inf for
-// rows without routes).
+// O = acc / l as BF16 (zero for rows without routes), LSE = (reference + log2 l) ln 2 (natural log, -inf for
+// rows without routes).  Each thread converts 16 consecutive elements of a row (four loads in flight).
 template <int D>
 __global__ void km_fwd_final_kernel(KfParams p, __nv_bfloat16 *o, float *lse) {
     if (*p.choice != 1) return;
+    const bool need_max = *p.need_max != 0;
     const int64_t n_rows = p.B * p.S_q * p.Hq;  // (b, q, h) rows of O
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    constexpr int kPer = D / 8;  // threads per row, 8 elements each
+    constexpr int kPer = D / 16;  // threads per row, 16 elements each
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_rows * kPer; i += stride) {
-        const int64_t row = i / kPer;
-        const int64_t h = row % p.Hq, bq = row / p.Hq;
-        const int64_t b = bq / p.S_q, q = bq % p.S_q;
-        const int64_t stat = row;  // [B, S_q, Hq]
-        const float2 ls = reinterpret_cast<const float2 *>(p.lrow)[stat];
-        const float l = ls.x;
+        const int64_t row = i / kPer;  // [B, S_q, Hq]: also the row statistics' index
+        const float4 *a4 = reinterpret_cast<const float4 *>(p.o_acc) + 4 * i;
+        float4 x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = a4[j];
+        const float2 ls = reinterpret_cast<const float2 *>(p.lrow)[row];
         const float inv = ls.y > 0.f ? 1.f / ls.y : 0.f;
-        const float4 *a4 = reinterpret_cast<const float4 *>(p.o_acc) + 2 * i;
-        const float4 x = a4[0], y = a4[1];
-        const float f[8] = {x.x * inv, x.y * inv, x.z * inv, x.w * inv, y.x * inv, y.y * inv, y.z * inv, y.w * inv};
-        reinterpret_cast<uint4 *>(o)[i] = f32x8_to_bf16(f);
-        if (i % kPer == 0)
-            lse[(b * p.Hq + h) * p.S_q + q] = l > 0.f ? (row_reference(p, *p.need_max != 0, stat) + __log2f(l)) * kLn2
-                                                       : -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float f[8] = {x[2 * j].x * inv, x[2 * j].y * inv, x[2 * j].z * inv, x[2 * j].w * inv,
+                                x[2 * j + 1].x * inv, x[2 * j + 1].y * inv, x[2 * j + 1].z * inv, x[2 * j + 1].w * inv};
+            reinterpret_cast<uint4 *>(o)[2 * i + j] = f32x8_to_bf16(f);
+        }
+        if (i % kPer == 0) {
+            const int64_t h = row % p.Hq, bq = row / p.Hq;
+            const int64_t b = bq / p.S_q, q = bq % p.S_q;
+            lse[(b * p.Hq + h) * p.S_q + q] = ls.x > 0.f ? (row_reference(p, need_max, row) + __log2f(ls.x)) * kLn2
+                                                         : -INFINITY;
+        }
     }
 }
 
