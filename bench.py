@@ -691,6 +691,28 @@ def run_route_producer(args):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    # The producer followed by the attention's route preprocessing on its rows, timed as one sequence: the
+    # rows arrive sorted, so route_rows copies them through.  Attention shape of the train-step workload
+    # (Hq32 Hkv4 D256) over the producer's rows; the tensors' contents are not read by the preprocessing.
+    att = W.WORKLOADS[HEADLINE_WORKLOAD]
+    aq = torch.empty((w.B, w.S_q, att.Hq, att.D), dtype=torch.bfloat16, device=dev)
+    akv = torch.empty((w.B, w.S_global, att.Hkv, att.D), dtype=torch.bfloat16, device=dev)
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    plan = None
+    for i in range(args.steps + max(1, args.warmup)):
+        timed = i >= max(1, args.warmup)
+        flush.fill_(i & 0xFF)
+        ev = pev[i - max(1, args.warmup)] if timed else None
+        step(ev)
+        plan = qsa.preprocess(aq, akv, akv, ids, att.softmax_scale, routes_sorted=True)
+        if ev:
+            ev[2].record()
+    torch.cuda.synchronize()
+    plan.device_status()
+    del plan, aq, akv
+    with_pre_ms = float(np.mean([e[0].elapsed_time(e[2]) for e in pev]))
+    pre_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in pev]))
+
     local_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in events]))
     score_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in sev]))
     sel_ms = max(local_ms - score_ms, 1e-6)  # the selection and the launch between the kernels
@@ -759,6 +781,11 @@ def run_route_producer(args):
             "useful_flop_per_step": flop,
         },
         "breakdown_ms": {"index_scores": round(score_ms, 4), "selection": round(sel_ms, 4)},
+        "with_preprocess": {
+            "ms_per_step": round(with_pre_ms, 4), "preprocess_ms": round(pre_ms, 4),
+            "step": "producer, then qsa_preprocess of its route rows (QSA_ROUTES_SORTED: copied through)",
+            "attention": f"{att.name}: B{w.B} S{w.S_q} Hq{att.Hq} Hkv{att.Hkv} D{att.D}, K={W_} producer slots",
+        },
         "roofline": roofline,
         "kernels": kernels,
         "cpu_baseline": cpu,

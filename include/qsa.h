@@ -85,7 +85,14 @@ typedef struct qsa_problem {
     int64_t k_stride[4];
     int64_t v_stride[4];
     int64_t r_stride[3];
+    uint32_t flags; /* 0, or QSA_ROUTES_SORTED */
 } qsa_problem;
+
+/* qsa_problem.flags: every row's valid IDs are strictly ascending and come before its invalid slots (as
+ * qsa_select_token_ids writes its rows).  qsa_preprocess then checks that on each row and copies such rows
+ * through instead of sorting them; a row found unsorted is sorted as usual, so the flag never changes a
+ * result, only the time (without it, the check is skipped: it would slow unsorted rows down). */
+#define QSA_ROUTES_SORTED 1u
 
 /* Validates a problem without touching the device. */
 QSA_API qsa_status qsa_check_problem(const qsa_problem *problem);

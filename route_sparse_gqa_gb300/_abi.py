@@ -57,8 +57,11 @@ class Problem(ctypes.Structure):
         ("Hkv", ctypes.c_int64), ("D", ctypes.c_int64), ("K", ctypes.c_int64),
         ("route_bits", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
         ("q_stride", ctypes.c_int64 * 4), ("k_stride", ctypes.c_int64 * 4), ("v_stride", ctypes.c_int64 * 4),
-        ("r_stride", ctypes.c_int64 * 3),
+        ("r_stride", ctypes.c_int64 * 3), ("flags", ctypes.c_uint32),
     ]
+
+
+ROUTES_SORTED = 1  # Problem.flags: rows already sorted and unique, invalid slots last
 
 
 class RouteProblem(ctypes.Structure):

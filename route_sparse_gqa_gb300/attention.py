@@ -59,7 +59,7 @@ def _check_inputs(query, key, value, routes):
         raise QSAError(_INVALID, "all tensors must be on the same device")
 
 
-def make_problem(query, key, value, routes, softmax_scale) -> _abi.Problem:
+def make_problem(query, key, value, routes, softmax_scale, routes_sorted: bool = False) -> _abi.Problem:
     B, S_q, Hq, D = query.shape
     _, S_kv, Hkv, _ = key.shape
     p = _abi.Problem()
@@ -72,6 +72,7 @@ def make_problem(query, key, value, routes, softmax_scale) -> _abi.Problem:
             arr[i] = s
     for i, s in enumerate(routes.stride()):
         p.r_stride[i] = s
+    p.flags = _abi.ROUTES_SORTED if routes_sorted else 0
     return p
 
 
@@ -108,11 +109,13 @@ class RoutePlan:
         _abi.check(_abi.load().qsa_read_device_status(self.workspace.data_ptr(), _stream_handle(self.workspace.device)))
 
 
-def preprocess(query, key, value, selected_token_ids, softmax_scale=None) -> RoutePlan:
+def preprocess(query, key, value, selected_token_ids, softmax_scale=None, routes_sorted: bool = False) -> RoutePlan:
+    """Route preprocessing.  routes_sorted: the rows' valid IDs already ascend with invalid slots last (as
+    select_qsa_token_ids returns them); rows found so are copied through (the result is the same either way)."""
     _check_inputs(query, key, value, selected_token_ids)
     scale = resolve_scale(softmax_scale, query.shape[-1])
     lib = _abi.load()
-    p = make_problem(query, key, value, selected_token_ids, scale)
+    p = make_problem(query, key, value, selected_token_ids, scale, routes_sorted)
     _abi.check(lib.qsa_check_problem(p))
     n = lib.qsa_workspace_bytes(p)
     ws = torch.empty(n, dtype=torch.uint8, device=query.device)

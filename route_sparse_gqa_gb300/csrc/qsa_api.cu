@@ -43,6 +43,7 @@ qsa_status validate(const qsa_problem *p) {
                     (double)p->softmax_scale);
     if (p->route_bits != 32 && p->route_bits != 64)
         return fail(QSA_ERR_INVALID_ARGUMENT, "route_bits must be 32 or 64 (got %d)", p->route_bits);
+    if (p->flags & ~QSA_ROUTES_SORTED) return fail(QSA_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", p->flags);
     if (p->D != 64 && p->D != 128 && p->D != kHeadDim)
         return fail(QSA_ERR_UNSUPPORTED, "head dim D=%lld: 64, 128 or 256 is supported", (long long)p->D);
     if (p->S_kv > 2147483647LL) return fail(QSA_ERR_UNSUPPORTED, "S_kv=%lld exceeds 2^31-1", (long long)p->S_kv);
@@ -451,6 +452,7 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
     r.rs2 = p->r_stride[2];
     r.ids = at<int32_t>(ws, L.off_ids);
     r.counts = at<int32_t>(ws, L.off_counts);
+    r.try_sorted = (p->flags & QSA_ROUTES_SORTED) != 0;
     e = launch_route_rows(r, stream);
     if (e != cudaSuccess) return cuda_fail(e, "route_rows launch");
     const int32_t *choice = nullptr;

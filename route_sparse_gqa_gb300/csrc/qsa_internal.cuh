@@ -102,6 +102,7 @@ struct RowsArgs {
     int64_t rs0, rs1, rs2;
     int32_t *ids;     // [B*S_q, K]
     int32_t *counts;  // [B*S_q]
+    bool try_sorted;  // QSA_ROUTES_SORTED: copy rows found sorted through
 };
 cudaError_t launch_route_rows(const RowsArgs &a, cudaStream_t s);
 

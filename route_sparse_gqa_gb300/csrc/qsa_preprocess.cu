@@ -40,7 +40,7 @@ constexpr int kRowMaxWindows = 8;        // still wider rows fall back to the bi
 constexpr size_t kRowSmem = kRowMapKeys + (size_t)kRowMapKeys / 32 * 8 > (size_t)kRowWindowBits / 32 * 8
                                 ? kRowMapKeys + (size_t)kRowMapKeys / 32 * 8
                                 : (size_t)kRowWindowBits / 32 * 8;
-constexpr int kRowCache = 16;          // route slots per thread kept in registers (K <= 16 * kRowThreads)
+constexpr int kRowCache = 17;          // route slots per thread kept in registers (K <= 17 * kRowThreads)
 
 __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -91,10 +91,14 @@ __device__ __forceinline__ uint32_t flag_nibble(uint32_t w) { return ((w * 0x002
 // with repeats gone, in coalesced stores.  Cost O(K + range/16) for the map,
 // O(K + range/32) per bitmap window; rows whose ids span more than
 // kRowMaxWindows windows use the bitonic sort instead.
+template <bool kTrySorted>
 __global__ void __launch_bounds__(kRowThreads, 8) route_rows_kernel(RowsArgs a, int P) {
     extern __shared__ __align__(16) uint32_t rsm[];  // map + words + offsets, bitmap + offsets, or bitonic buffer [P]
     __shared__ int warp_tot[33];
     __shared__ int64_t red_lo[kRowThreads / 32], red_hi[kRowThreads / 32];
+    __shared__ int32_t lane0[kRowCache + 1][kRowThreads / 32];  // cached slot j of each warp's lane 0
+    __shared__ int n_valid;
+    __shared__ bool red_sorted[kRowThreads / 32];
     const int64_t row = blockIdx.x;
     const int64_t b = row / a.S_q, q = row % a.S_q;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
@@ -126,6 +130,30 @@ __global__ void __launch_bounds__(kRowThreads, 8) route_rows_kernel(RowsArgs a, 
             }
         }
     }
+    // With QSA_ROUTES_SORTED (kTrySorted), rows that arrive sorted (valid ids strictly ascending, every
+    // invalid slot after them, as the route producer writes them) are copied through.  Slot i is checked against slot i + 1: the next lane's slot j
+    // (shuffles; the verdict of each warp rides on the range reduction's barrier), or for lane 31 the next
+    // warp's lane 0 (slot j + 1 of warp 0 after the last warp), checked only when every warp passed.
+    bool warp_sorted = false;
+    if (kTrySorted && cached) {
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < kRowCache; ++j) {
+            const int32_t x = cache[j];
+            const int32_t y = __shfl_down_sync(0xffffffffu, x, 1);
+            bad |= lane < 31 && ((y >= 0 && x < 0) || (x >= 0 && y >= 0 && y <= x));
+            // The thread's own slots, 128 apart, must ascend too: rejects most unsorted rows before any
+            // exchange between warps.
+            if (j + 1 < kRowCache) bad |= cache[j + 1] >= 0 && (x < 0 || cache[j + 1] <= x);
+        }
+        warp_sorted = !__any_sync(0xffffffffu, bad);
+        if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < kRowCache; ++j) lane0[j][warp] = cache[j];
+        }
+        if (tid < nwarps) lane0[kRowCache][tid] = -1;
+        if (tid == 0) n_valid = 0;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
@@ -134,8 +162,36 @@ __global__ void __launch_bounds__(kRowThreads, 8) route_rows_kernel(RowsArgs a, 
     if (lane == 0) {
         red_lo[warp] = lo;
         red_hi[warp] = hi;
+        if (kTrySorted) red_sorted[warp] = warp_sorted;
     }
     __syncthreads();
+    if (kTrySorted && cached) {
+        bool all = true;
+        for (int w = 0; w < nwarps; ++w) all &= red_sorted[w];
+        if (all) {  // uniform over the block
+            bool bad = false;
+            int nv = 0;
+#pragma unroll
+            for (int j = 0; j < kRowCache; ++j) {
+                const int32_t x = cache[j];
+                const int32_t y = warp + 1 < nwarps ? lane0[j][warp + 1] : lane0[j + 1][0];
+                bad |= lane == 31 && ((y >= 0 && x < 0) || (x >= 0 && y >= 0 && y <= x));
+                nv += x >= 0;
+            }
+            if (__syncthreads_and(!bad)) {
+                atomicAdd(&n_valid, nv);
+                __syncthreads();
+                const int total = n_valid;
+#pragma unroll
+                for (int j = 0; j < kRowCache; ++j) {
+                    const int64_t i = tid + (int64_t)j * blockDim.x;
+                    if (i < a.K) out[i] = cache[j];  // -1 for invalid slots, which all come after the valid ones
+                }
+                if (tid == 0) a.counts[row] = total;
+                return;
+            }
+        }
+    }
     lo = red_lo[0];
     hi = red_hi[0];
     for (int w = 1; w < nwarps; ++w) {
@@ -460,10 +516,13 @@ cudaError_t launch_route_rows(const RowsArgs &a, cudaStream_t s) {
     while (P < a.K) P <<= 1;
     const size_t smem = std::max<size_t>((size_t)P * sizeof(int32_t), kRowSmem);
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(route_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(route_rows_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(route_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    route_rows_kernel<<<(unsigned)(a.B * a.S_q), kRowThreads, smem, s>>>(a, P);
+    if (a.try_sorted) route_rows_kernel<true><<<(unsigned)(a.B * a.S_q), kRowThreads, smem, s>>>(a, P);
+    else route_rows_kernel<false><<<(unsigned)(a.B * a.S_q), kRowThreads, smem, s>>>(a, P);
     return cudaGetLastError();
 }
 

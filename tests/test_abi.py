@@ -48,6 +48,21 @@ def test_header_compiles_as_c():
     assert r.returncode == 0, r.stderr
 
 
+def test_problem_struct_layout_matches_the_header(tmp_path):
+    """The binding's ctypes structs have the C structs' sizes and field offsets."""
+    fields = [f for f, _ in _abi.Problem._fields_]
+    src = (f'#include <stdio.h>\n#include <stddef.h>\n#include "{HEADER}"\nint main(void) {{\n'
+           '  printf("%zu", sizeof(qsa_problem));\n' +
+           "".join(f'  printf(" %zu", offsetof(qsa_problem, {f}));\n' for f in fields) + '  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    r = subprocess.run(["gcc", "-x", "c", "-std=c99", "-I/usr/local/cuda/include", "-o", str(exe), "-"],
+                       input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(_abi.Problem)
+    assert got[1:] == [getattr(_abi.Problem, f).offset for f in fields]
+
+
 def good_problem(**kw):
     p = _abi.Problem()
     B, S_q, S_kv, Hq, Hkv, D, K = 2, 100, 300, 16, 2, 256, 50
@@ -79,6 +94,8 @@ def good_problem(**kw):
     ({"softmax_scale": math.inf}, 1),
     ({"softmax_scale": math.nan}, 1),
     ({"route_bits": 16}, 1),
+    ({"flags": 1}, 0),
+    ({"flags": 2}, 1),
     ({"D": 128, "q_stride": (100 * 16 * 128, 16 * 128, 128, 1), "k_stride": (300 * 2 * 128, 2 * 128, 128, 1),
       "v_stride": (300 * 2 * 128, 2 * 128, 128, 1)}, 0),
     ({"D": 96}, 2),

@@ -272,6 +272,54 @@ def test_route_sets_at_sort_method_boundaries(K):
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
 
 
+@pytest.mark.parametrize("K", [96, 2176, 2177])
+def test_route_sets_presorted_rows(K):
+    """Rows that arrive sorted (as the route producer writes them), and rows that only nearly are (a repeat,
+    an invalid slot before a valid one, descending ids, an id at S_kv, out-of-range and huge tails): bit-exact
+    against the oracle's route sets with and without the rows-sorted flag (which copies sorted rows through
+    and must sort the others as usual), on both sides of route_rows' register-row limit (17 x 128 slots)."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    rng = np.random.default_rng(91 + K)
+    S_kv = 50_000
+    n_valid = min(K - 8, 1500)
+    rows = []
+    for kind in range(8):
+        ids = np.sort(rng.choice(S_kv, size=n_valid, replace=False)).astype(np.int64)
+        r = np.full(K, -1, np.int64)
+        r[:n_valid] = ids
+        if kind == 1:  # out-of-range tail after the sorted valid ids (invalid, still after them)
+            r[n_valid:] = S_kv + rng.integers(0, 5, size=K - n_valid)
+        elif kind == 2:  # a repeat
+            r[n_valid // 2] = r[n_valid // 2 - 1]
+        elif kind == 3:  # an invalid slot before a valid one
+            r[n_valid // 3] = -5
+        elif kind == 4:  # descending
+            r[:n_valid] = ids[::-1]
+        elif kind == 5:  # id S_kv (invalid) in the middle of the valid run
+            r[n_valid // 4] = S_kv
+        elif kind == 6:  # empty row
+            r[:] = -1
+        elif kind == 7:  # huge int64 tail
+            r[n_valid:] = 2**40 + 1
+        rows.append(r)
+    routes = np.stack(rows)[None]
+    S_q = routes.shape[1]
+    dev = torch.device("cuda:0")
+    q = torch.zeros(1, S_q, 16, 256, dtype=torch.bfloat16, device=dev)
+    k = torch.zeros(1, S_kv, 2, 256, dtype=torch.bfloat16, device=dev)
+    for dtype in (np.int64, np.int32):
+        rt = routes.astype(dtype) if dtype == np.int64 else np.where(routes > 2**31 - 1, -1, routes).astype(np.int32)
+        ids_ref, counts_ref = oracle.route_sets(rt, S_kv)
+        for hint in (False, True):  # QSA_ROUTES_SORTED: sorted rows copied through, the others sorted as usual
+            plan = qsa.preprocess(q, k, k, torch.from_numpy(rt).to(dev), routes_sorted=hint)
+            ids, counts = plan.route_sets()
+            assert np.array_equal(counts.cpu().numpy(), counts_ref), (dtype, hint)
+            assert np.array_equal(ids.cpu().numpy(), ids_ref), (dtype, hint)
+
+
 def test_repeated_calls_share_one_workspace():
     """The tile and key-major kernels take their work from queues whose counters
     live in the workspace and are reset by the last CTA of every launch.  Calls

@@ -275,7 +275,8 @@ def test_select_token_ids_edge_shapes(B, S_q, H, D, c, budget, offset, lens, S_g
 
 
 def test_rows_are_already_route_sets():
-    """The producer's rows pass through the attention preprocessing unchanged."""
+    """The producer's rows pass through the attention preprocessing unchanged (with the rows-sorted flag the
+    preprocessing copies them through)."""
     import torch
 
     import route_sparse_gqa_gb300 as qsa
@@ -288,7 +289,7 @@ def test_rows_are_already_route_sets():
     B, S, Hq, Hkv, D = w.B, w.S_q, 8, 1, 256
     q = torch.zeros(B, S, Hq, D, dtype=torch.bfloat16, device=dev)
     kv = torch.zeros(B, S, Hkv, D, dtype=torch.bfloat16, device=dev)
-    plan = qsa.preprocess(q, kv, kv, routes)
+    plan = qsa.preprocess(q, kv, kv, routes, routes_sorted=True)
     sets, counts = plan.route_sets()
     torch.cuda.synchronize()
     assert np.array_equal(sets.cpu().numpy(), ids)
