@@ -8,9 +8,9 @@ seconds, so:
 * dK and dV on sampled keys, recomputed from every row that routes to them:
   keys late in the sequence (few routing rows) and the hottest ones -- the
   first routed key (block 0, routed by thousands of rows on the long
-  workloads: the most reductions and the most work items per chunk) and the
-  last routed key (the last rows' own block; past 2^31 bytes of K/V on the
-  long-K/V workload);
+  workloads: the most reductions and the most work items per chunk), the two
+  keys with the most routing rows, and the last routed key (the last rows'
+  own block; past 2^31 bytes of K/V on the long-K/V workload);
 * properties that hold at any size on the whole output: sum_j dK_j = 0 and
   sum_j dV_j = sum of dO over the group's non-empty rows (fp32 accumulators),
   and exact zeros for keys no row routes to.
@@ -42,9 +42,11 @@ def _sample_rows(rng, counts_b, n):
     return np.array(sorted(rows))
 
 
-def _sample_keys(rng, ids_b, counts_b, S_kv, n, max_rows=1500):
+def _sample_keys(rng, ids_b, counts_b, S_kv, n):
     """Keys late in the sequence (few routing rows, so the oracle stays fast),
-    the first and the last routed key (the hottest and the highest), plus one
+    the first and the last routed key (block 0 and the highest key), the two
+    keys the most rows route to (the most reductions: block 0 again, or on the
+    packed workload the first blocks of the longest documents), plus one
     never-routed key if there is one."""
     used = np.zeros(S_kv, bool)
     valid = ids_b[ids_b >= 0]
@@ -54,6 +56,8 @@ def _sample_keys(rng, ids_b, counts_b, S_kv, n, max_rows=1500):
     keys = set(rng.choice(late, size=min(n, late.size), replace=False).tolist())
     if cand.size:
         keys.update((int(cand[0]), int(cand[-1])))
+        hot = np.bincount(valid, minlength=S_kv)
+        keys.update(int(x) for x in np.argsort(-hot, kind="stable")[:2])
     keys = np.array(sorted(keys), dtype=np.int64)
     unused = np.nonzero(~used)[0]
     return keys, unused

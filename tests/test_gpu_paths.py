@@ -48,6 +48,8 @@ SHAPES = [
     (76, 2, 300, 520, 16, 2, 448, 256, "blocks", np.int64),   # two batch rows, lists over several work items
     (73, 1, 90, 200, 32, 2, 40, 256, "random", np.int32),     # G = 16
     (74, 1, 120, 256, 16, 2, 64, 128, "blocks", np.int32),    # D = 128
+    (78, 1, 70, 260, 64, 2, 60, 128, "random", np.int32),     # G = 32 (four queries per group), D = 128
+    (79, 2, 50, 200, 64, 1, 40, 256, "random", np.int64),    # G = 64 (two queries per group)
 ]
 
 
