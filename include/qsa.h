@@ -115,17 +115,26 @@ QSA_API size_t qsa_workspace_bytes(const qsa_problem *problem);
 /* Route preprocessing (fa4_qsa _preprocess and _block_kinds/_compact_blocks
  * play this role on the pages): validates every route ID against [0, S_kv) in
  * its own width before any narrowing, drops duplicates, sorts each row
- * ascending, and builds the per-query-tile key lists and membership masks the
- * attention kernels read.  Writes only into `workspace`, which the forward and
- * backward calls then read; reuse it for both as long as the routes are
- * unchanged.  No host synchronisation. */
+ * ascending (rows already sorted are copied through when problem->flags has
+ * QSA_ROUTES_SORTED), and builds what the attention kernels read: for each
+ * aligned 64-key chunk, the query rows that route into it with their key masks
+ * (the key-major kernels' work), and, when a tile kernel will run, per query
+ * tile the union of its rows' keys with membership masks.  It also decides on
+ * the device, from counts of both, which kernel family the forward and the
+ * backward use (they compute the same function).  Writes only into
+ * `workspace`, which the forward and backward calls then read; reuse it for
+ * both as long as the routes are unchanged.  No host synchronisation. */
 QSA_API qsa_status qsa_preprocess(const qsa_problem *problem, const void *routes, void *workspace, size_t ws_bytes,
                           cudaStream_t stream);
 
 /* Forward pass (flex_sparse_gqa_attention / fa4_sparse_gqa_attention returns O;
  * the per-row LSE is kept for the backward pass).  Needs a workspace filled by
  * qsa_preprocess for the same problem; the preprocessed routes are only read,
- * the work queue counters are used and left reset.  o and lse are written in
+ * the work queue counters are used and left reset.  The key-major forward
+ * accumulates O in fp32 through L2 and normalises once at the end; its
+ * exponent reference per row is a Cauchy-Schwarz bound on the row's scores
+ * when that keeps the row's largest weight above 2^-64, else the row maximum
+ * from an extra pass (the same function either way, up to rounding).  o and lse are written in
  * full (rows with no valid route get O = 0 and LSE = -inf); they must not
  * overlap q, k, v or the workspace. */
 QSA_API qsa_status qsa_forward(const qsa_problem *problem, void *workspace, size_t ws_bytes, const void *q,
