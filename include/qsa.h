@@ -85,7 +85,7 @@ typedef struct qsa_problem {
     int64_t k_stride[4];
     int64_t v_stride[4];
     int64_t r_stride[3];
-    uint32_t flags; /* 0, or QSA_ROUTES_SORTED */
+    uint32_t flags; /* 0, or QSA_ROUTES_SORTED | QSA_DETERMINISTIC_FORWARD */
 } qsa_problem;
 
 /* qsa_problem.flags: every row's valid IDs are strictly ascending and come before its invalid slots (as
@@ -93,6 +93,12 @@ typedef struct qsa_problem {
  * through instead of sorting them; a row found unsorted is sorted as usual, so the flag never changes a
  * result, only the time (without it, the check is skipped: it would slow unsorted rows down). */
 #define QSA_ROUTES_SORTED 1u
+/* qsa_problem.flags: qsa_forward's O and LSE bitwise reproducible.  The key-major forward sums each row's
+ * output over work items in fp32 in whatever order the items finish, so repeated calls agree within
+ * rounding only; with this flag the preprocessing always picks the tile forward (every output row computed
+ * by one CTA in a fixed order), slower on routes that a query tile shares poorly.  Together with
+ * qsa_backward_deterministic the whole step is reproducible. */
+#define QSA_DETERMINISTIC_FORWARD 2u
 
 /* Validates a problem without touching the device. */
 QSA_API qsa_status qsa_check_problem(const qsa_problem *problem);

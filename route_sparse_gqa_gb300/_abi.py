@@ -62,6 +62,7 @@ class Problem(ctypes.Structure):
 
 
 ROUTES_SORTED = 1  # Problem.flags: rows already sorted and unique, invalid slots last
+DETERMINISTIC_FORWARD = 2  # Problem.flags: bitwise reproducible forward (the tile kernels)
 
 
 class RouteProblem(ctypes.Structure):

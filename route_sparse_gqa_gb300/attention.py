@@ -59,7 +59,8 @@ def _check_inputs(query, key, value, routes):
         raise QSAError(_INVALID, "all tensors must be on the same device")
 
 
-def make_problem(query, key, value, routes, softmax_scale, routes_sorted: bool = False) -> _abi.Problem:
+def make_problem(query, key, value, routes, softmax_scale, routes_sorted: bool = False,
+                 deterministic_forward: bool = False) -> _abi.Problem:
     B, S_q, Hq, D = query.shape
     _, S_kv, Hkv, _ = key.shape
     p = _abi.Problem()
@@ -72,7 +73,7 @@ def make_problem(query, key, value, routes, softmax_scale, routes_sorted: bool =
             arr[i] = s
     for i, s in enumerate(routes.stride()):
         p.r_stride[i] = s
-    p.flags = _abi.ROUTES_SORTED if routes_sorted else 0
+    p.flags = (_abi.ROUTES_SORTED if routes_sorted else 0) | (_abi.DETERMINISTIC_FORWARD if deterministic_forward else 0)
     return p
 
 
@@ -109,13 +110,15 @@ class RoutePlan:
         _abi.check(_abi.load().qsa_read_device_status(self.workspace.data_ptr(), _stream_handle(self.workspace.device)))
 
 
-def preprocess(query, key, value, selected_token_ids, softmax_scale=None, routes_sorted: bool = False) -> RoutePlan:
+def preprocess(query, key, value, selected_token_ids, softmax_scale=None, routes_sorted: bool = False,
+               deterministic_forward: bool = False) -> RoutePlan:
     """Route preprocessing.  routes_sorted: the rows' valid IDs already ascend with invalid slots last (as
-    select_qsa_token_ids returns them); rows found so are copied through (the result is the same either way)."""
+    select_qsa_token_ids returns them); rows found so are copied through (the result is the same either way).
+    deterministic_forward: the forward's O and LSE bitwise reproducible (the tile kernels run)."""
     _check_inputs(query, key, value, selected_token_ids)
     scale = resolve_scale(softmax_scale, query.shape[-1])
     lib = _abi.load()
-    p = make_problem(query, key, value, selected_token_ids, scale, routes_sorted)
+    p = make_problem(query, key, value, selected_token_ids, scale, routes_sorted, deterministic_forward)
     _abi.check(lib.qsa_check_problem(p))
     n = lib.qsa_workspace_bytes(p)
     ws = torch.empty(n, dtype=torch.uint8, device=query.device)
@@ -183,7 +186,7 @@ class _RouteShape:
 class _QSAFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, query, key, value, routes, softmax_scale, deterministic):
-        plan = preprocess(query, key, value, routes, softmax_scale)
+        plan = preprocess(query, key, value, routes, softmax_scale, deterministic_forward=deterministic)
         o, lse = forward(plan, query, key, value)
         ctx.save_for_backward(query, key, value, o, lse)
         ctx.plan = plan
@@ -200,7 +203,7 @@ class _QSAFunction(torch.autograd.Function):
 def qsa_attention(query, key, value, selected_token_ids, softmax_scale=None, deterministic: bool = False):
     """Exact route-set sparse GQA attention; differentiable in query/key/value
     (first order).  Returns BF16 ``[B,S_q,Hq,D]``.  ``deterministic`` makes the
-    backward bitwise reproducible."""
+    forward and the backward bitwise reproducible."""
     return _QSAFunction.apply(query, key, value, selected_token_ids, softmax_scale, deterministic)
 
 

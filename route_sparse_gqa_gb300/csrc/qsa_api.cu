@@ -43,7 +43,8 @@ qsa_status validate(const qsa_problem *p) {
                     (double)p->softmax_scale);
     if (p->route_bits != 32 && p->route_bits != 64)
         return fail(QSA_ERR_INVALID_ARGUMENT, "route_bits must be 32 or 64 (got %d)", p->route_bits);
-    if (p->flags & ~QSA_ROUTES_SORTED) return fail(QSA_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", p->flags);
+    if (p->flags & ~(QSA_ROUTES_SORTED | QSA_DETERMINISTIC_FORWARD))
+        return fail(QSA_ERR_INVALID_ARGUMENT, "unknown flags 0x%x", p->flags);
     if (p->D != 64 && p->D != 128 && p->D != kHeadDim)
         return fail(QSA_ERR_UNSUPPORTED, "head dim D=%lld: 64, 128 or 256 is supported", (long long)p->D);
     if (p->S_kv > 2147483647LL) return fail(QSA_ERR_UNSUPPORTED, "S_kv=%lld exceeds 2^31-1", (long long)p->S_kv);
@@ -464,7 +465,7 @@ qsa_status qsa_preprocess(const qsa_problem *p, const void *routes, void *ws, si
         const AttnArgs a = attn_args(p, L, ws, nullptr, nullptr, nullptr);
         const bool tile_bwd_ok = tc_backward_supported() && tc_backward_shape_ok(a, tile_args(p, L, ws));
         e = launch_km_choose(c.tile_keys, p->B * L.n_tiles, c.list_start, p->B * L.NC, L.T, p->D, tile_bwd_ok,
-                             c.meta + 4, stream);
+                             (p->flags & QSA_DETERMINISTIC_FORWARD) != 0, c.meta + 4, stream);
         if (e != cudaSuccess) return cuda_fail(e, "path choice launch");
         choice = c.meta + 4;
     }

@@ -875,13 +875,14 @@ bool km_forward_shape_ok(const AttnArgs &a) {
 }
 
 cudaError_t launch_km_choose(const int32_t *tile_keys, int64_t n_tiles, const int32_t *list_start,
-                             int64_t n_lists, int64_t slots, int64_t D, bool tile_bwd_ok, int32_t *choice,
-                             cudaStream_t s) {
+                             int64_t n_lists, int64_t slots, int64_t D, bool tile_bwd_ok, bool tile_fwd_only,
+                             int32_t *choice, cudaStream_t s) {
     // Backward: a key-major group costs about kBwdRatio tile chunks (per unit and KV head: tile 33-34 ns and
     // key-major 35-41 ns at D = 256 on train-step and right-padded; 24 against 32 ns at D = 128).
     const int bwd_num = D == 128 ? 27 : 6, bwd_den = tile_bwd_ok ? (D == 128 ? 20 : 5) : 0;
     km_choose_kernel<<<1, 1024, 0, s>>>(tile_keys, n_tiles, list_start, n_lists, slots,
-                                        forced_path("QSA_DEBUG_FORWARD_PATH"), forced_path("QSA_DEBUG_BACKWARD_PATH"),
+                                        tile_fwd_only ? 0 : forced_path("QSA_DEBUG_FORWARD_PATH"),
+                                        forced_path("QSA_DEBUG_BACKWARD_PATH"),
                                         bwd_num, bwd_den, choice);
     return cudaGetLastError();
 }

@@ -99,10 +99,11 @@ struct KfArgs {
 constexpr int64_t kKeyNormWord = 64;
 bool km_forward_shape_ok(const AttnArgs &a);
 int forced_path(const char *env_var);  // debug override of a path choice: 0 tile, 1 key-major, -1 none
-// choice[0]: 1 = key-major forward; choice[1]: 1 = key-major backward (always 1 when !tile_bwd_ok).
+// choice[0]: 1 = key-major forward (never with tile_fwd_only); choice[1]: 1 = key-major backward (always 1
+// when !tile_bwd_ok).
 cudaError_t launch_km_choose(const int32_t *tile_keys, int64_t n_tiles, const int32_t *list_start,
-                             int64_t n_lists, int64_t slots, int64_t D, bool tile_bwd_ok, int32_t *choice,
-                             cudaStream_t s);
+                             int64_t n_lists, int64_t slots, int64_t D, bool tile_bwd_ok, bool tile_fwd_only,
+                             int32_t *choice, cudaStream_t s);
 cudaError_t launch_km_forward(const AttnArgs &a, const KfArgs &k, __nv_bfloat16 *o, float *lse, cudaStream_t s);
 
 bool tc_backward_supported();

@@ -95,7 +95,9 @@ def good_problem(**kw):
     ({"softmax_scale": math.nan}, 1),
     ({"route_bits": 16}, 1),
     ({"flags": 1}, 0),
-    ({"flags": 2}, 1),
+    ({"flags": 2}, 0),
+    ({"flags": 3}, 0),
+    ({"flags": 4}, 1),
     ({"D": 128, "q_stride": (100 * 16 * 128, 16 * 128, 128, 1), "k_stride": (300 * 2 * 128, 2 * 128, 128, 1),
       "v_stride": (300 * 2 * 128, 2 * 128, 128, 1)}, 0),
     ({"D": 96}, 2),

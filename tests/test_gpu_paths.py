@@ -74,6 +74,42 @@ def test_each_path_matches_oracle(shape, fwd, bwd, monkeypatch):
     assert_close("dV fp32", out["dv32"], dv_ref)
 
 
+def test_keymajor_forward_repeats_within_rounding_and_deterministic_flag(monkeypatch):
+    """The key-major forward sums each row's output over work items in fp32 in the order they finish:
+    repeated calls agree within the tolerance (and with the oracle).  With the deterministic-forward flag the
+    preprocessing picks the tile forward even when the key-major one is forced by the test hook, so repeated
+    calls, and with the deterministic backward the whole step, agree bit for bit."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+    from tests.qsa_testlib import bf16_to_device
+
+    monkeypatch.setenv("QSA_DEBUG_FORWARD_PATH", "keymajor")
+    q, k, v, do, routes = _case(80, 1, 600, 1500, 16, 2, 700, 256, "blocks", np.int32)
+    dev = torch.device("cuda:0")
+    qt, kt, vt, dot = (bf16_to_device(x, dev) for x in (q, k, v, do))
+    rt = torch.from_numpy(routes).to(dev)
+    o_ref, lse_ref = oracle.forward(f64(q), f64(k), f64(v), routes, 0.0625)
+    for det in (False, True):
+        plan = qsa.preprocess(qt, kt, vt, rt, 0.0625, deterministic_forward=det)
+        runs = []
+        for _ in range(3):
+            o, lse = qsa.forward(plan, qt, kt, vt)
+            grads = qsa.backward(plan, qt, kt, vt, o, lse, dot, deterministic=det)
+            runs.append([x.float().cpu().numpy() for x in (o, lse, *grads)])
+        plan.device_status()
+        for later in runs[1:]:
+            for name, a, b in zip(("O", "LSE", "dQ", "dK", "dV"), runs[0], later):
+                if det:
+                    assert np.array_equal(a, b, equal_nan=True), f"{name} differs between repeated calls"
+                elif name == "LSE":
+                    assert_lse_close(b.astype(np.float64), a.astype(np.float64))
+                else:
+                    assert_close(name + " repeat", b.astype(np.float64), a.astype(np.float64))
+        assert_close("O", runs[-1][0].astype(np.float64), o_ref)
+        assert_lse_close(runs[-1][1].astype(np.float64), lse_ref)
+
+
 def test_keymajor_forward_deterministic_backward(monkeypatch):
     """The key-major forward followed by the bitwise reproducible backward on the key-major path: two
     runs agree bit for bit and match the oracle."""
