@@ -87,6 +87,29 @@ def test_no_alloc_forward_matches_oracle_and_allocating_path(lib):
         assert_lse_close(got_lse, ll)
 
 
+def test_no_alloc_forward_keymajor_path(lib, monkeypatch):
+    """The same on the key-major forward (forced by the test hook) on the static array: reverse lists,
+    key norm bound, output pass and final division all in its forward part."""
+    import torch
+
+    import route_sparse_gqa_gb300 as qsa
+
+    monkeypatch.setenv("QSA_DEBUG_FORWARD_PATH", "keymajor")
+    dev = torch.device("cuda:0")
+    qb, kb, vb, routes_np, scale = _inputs("ragged")
+    q, k, v = (bf16_to_device(x, dev) for x in (qb, kb, vb))
+    routes = torch.from_numpy(routes_np).to(dev)
+    plan = qsa.preprocess(q, k, v, routes, scale)
+    o = torch.full((q.shape[0], q.shape[1], q.shape[2], q.shape[3]), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((q.shape[0], q.shape[2], q.shape[1]), float("nan"), dtype=torch.float32, device=dev)
+    for _ in range(2):
+        _abi.check(_no_alloc(lib, plan, routes, q, k, v, o, lse))
+        _abi.check(lib.qsa_read_no_alloc_status(torch.cuda.current_stream(dev).cuda_stream))
+        oo, ll = oracle.forward(f64(qb), f64(kb), f64(vb), routes_np, scale)
+        assert_close("O (key-major, no alloc)", o.float().cpu().numpy().astype(np.float64), oo)
+        assert_lse_close(lse.cpu().numpy().astype(np.float64), ll)
+
+
 def test_no_alloc_call_allocates_nothing(lib):
     import torch
 
