@@ -69,3 +69,35 @@ def test_job_rate_counts_every_replica():
     # two replicas of a 1e12-FLOP step in the slowest rank's 2 ms: 1000 TFLOP/s for the job
     assert abs(bench.job_tflops(1e12, 2, 2.0) - 1000.0) < 1e-9
     assert abs(bench.job_tflops(1e12, 1, 2.0) - 500.0) < 1e-9
+
+
+def test_executed_pairs_against_brute_force():
+    """The executed/useful pair counts of the two kernel families, recounted by brute force on a tiny case:
+    tile kernels = sum over T-query tiles of ceil(distinct keys / 64) chunks; key-major kernels = sum over
+    (query window, aligned 64-key chunk) of ceil(routing queries / T) groups; each chunk or group is 64 x 128
+    (query-head row, key) pairs, over the routed pairs times G."""
+    import numpy as np
+
+    from route_sparse_gqa_gb300 import workloads as W
+
+    w = W.Workload(99, "t", 1, 70, 300, 16, 2, 256, 12, np.int32, 0.0625, "t")
+    rng = np.random.default_rng(3)
+    ids = np.full((1, 70, 12), -1, np.int32)
+    counts = np.zeros((1, 70), np.int32)
+    for q in range(70):
+        n = int(rng.integers(0, 13))
+        ids[0, q, :n] = np.sort(rng.choice(300, size=n, replace=False))
+        counts[0, q] = n
+    got = bench.executed_pairs(w, ids, counts)
+    G, T = 8, 16
+    tiles = sum(-(-len(set(ids[0, t:t + T][ids[0, t:t + T] >= 0].tolist())) // 64) for t in range(0, 70, T))
+    # one window covers all 70 rows here (the window is thousands of rows)
+    per_chunk = {}
+    for q in range(70):
+        for c in set((ids[0, q, :counts[0, q]] // 64).tolist()):
+            per_chunk[c] = per_chunk.get(c, 0) + 1
+    groups = sum(-(-n // T) for n in per_chunk.values())
+    useful = int(counts.sum()) * G
+    assert got["tile_chunks"] == tiles and got["keymajor_groups"] == groups
+    assert abs(got["tile_over_useful"] - round(tiles * 64 * 128 / useful, 3)) < 1e-9
+    assert abs(got["keymajor_over_useful"] - round(groups * 64 * 128 / useful, 3)) < 1e-9
