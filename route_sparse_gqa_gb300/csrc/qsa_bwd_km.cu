@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_bwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
                     for (int kb = 0; kb < L::kPanels; ++kb) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_bwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
                     for (int kb = 0; kb < L::kPanels; ++kb) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_bwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
                     for (int h = 0; h < L::kHalves; ++h) {
 #pragma unroll
                         for (int kk = 0; kk < kTileRows / 16; ++kk) {
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) km_bwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 if (lane == 0) {
-#pragma unroll
+#pragma unroll 1
                     for (int h = 0; h < L::kHalves; ++h) {
 #pragma unroll
                         for (int kk = 0; kk < kTileRows / 16; ++kk) {

@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) km_fwd_max_kernel(const __grid
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t qa = sbase + L::kOffQ + st * L::kTileBytes;
-#pragma unroll
+#pragma unroll 1
                     for (int kb = 0; kb < L::kPanels; ++kb)
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kOutThreads, 1) km_fwd_out_kernel(const __grid
                     return false;
                 tc_fence_after();
                 const uint32_t qa = sbase + L::kOffQ + st * L::kTileBytes;
-#pragma unroll
+#pragma unroll 1
                 for (int kb = 0; kb < L::kPanels; ++kb)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
