@@ -35,6 +35,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -188,14 +189,48 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(src: bytes) -> bytes:
+    """C/C++ source with its // and /* */ comments removed and every run of white space reduced to one
+    space (string and character literals are kept), so that editing comments or layout alone leaves
+    the hash below, and the measurements recorded against it, valid."""
+    out = bytearray()
+    i, n = 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in (0x22, 0x27):  # a string or character literal, copied through with its escapes
+            out.append(c)
+            i += 1
+            while i < n:
+                d = src[i]
+                out.append(d)
+                i += 1
+                if d == 0x5C and i < n:
+                    out.append(src[i])
+                    i += 1
+                elif d == c:
+                    break
+        elif src.startswith(b"//", i):
+            j = src.find(b"\n", i)
+            i = n if j < 0 else j
+        elif src.startswith(b"/*", i):
+            j = src.find(b"*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(0x20)
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(rb"\s+", b" ", bytes(out)).strip()
+
+
 def kernel_source_hash(kernel: str | None = None) -> str:
-    """Hash of the kernel's source files (every CUDA source when `kernel` is None)."""
+    """Hash of the code of the kernel's source files, comments and layout aside (every CUDA source when
+    `kernel` is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "route_sparse_gqa_gb300", "csrc")
     names = KERNEL_SOURCES.get(kernel) if kernel else None
     for name in sorted(names or os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+            h.update(name.encode() + b"\0" + _code_only(f.read()) + b"\0")
     return h.hexdigest()[:16]
 
 

@@ -65,6 +65,28 @@ def test_recorded_traffic_only_for_unchanged_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("k") is None
 
 
+def test_recorded_traffic_survives_comment_and_layout_edits(tmp_path, monkeypatch):
+    """The recorded DRAM traffic belongs to the code: editing a comment or the layout keeps it, changing a
+    token (also one inside a string literal, or one that looks like a comment marker there) drops it."""
+    csrc = tmp_path / "route_sparse_gqa_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    base = 'int a = f(x);  // add one\nconst char *s = "// not a comment";\n/* block */ char c = \'"\';\n'
+    (csrc / "k.cu").write_text(base)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", {"k": ["k.cu"]})
+    rec = {"k": {"bytes_per_launch": 777, "source_hash": bench.kernel_source_hash("k")}}
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps(rec))
+    same = ('// a new leading comment\nint a =   f(x);\n\nconst char *s = "// not a comment";  /* more */\n'
+            'char c = \'"\';  // the quote character\n')
+    (csrc / "k.cu").write_text(same)
+    assert bench.recorded_traffic("k") == 777
+    for changed in (base.replace("f(x)", "f(y)"), base.replace('"// not a comment"', '"// changed"'),
+                    base.replace("char c", "int c")):
+        (csrc / "k.cu").write_text(changed)
+        assert bench.recorded_traffic("k") is None
+
+
 def test_job_rate_counts_every_replica():
     # two replicas of a 1e12-FLOP step in the slowest rank's 2 ms: 1000 TFLOP/s for the job
     assert abs(bench.job_tflops(1e12, 2, 2.0) - 1000.0) < 1e-9
